@@ -1,0 +1,282 @@
+"""CPU oracle for routed block-sparse self-attention (TEST INFRASTRUCTURE ONLY).
+
+Only the tests, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline
+leg may import this module. The CUDA library never calls it, and it shares no
+code with the CUDA library: it is a plain, slow, fp64 restatement of what the
+layer computes, written so that a reader can check it against the pages by eye.
+
+What the pages fix, and where:
+
+* "MiniMax H3 runs on single 4090 with 4.44x speedup over dense execution",
+  third paragraph: the layer attends over a [1, 38247, 56, 128] bf16 tensor;
+  Sol-Attn runs with tau = 1.0, a diagonal threshold, an exact KV sink for the
+  prefix and compressed prefix queries; the first steps and layers run dense.
+  (The Hebrew version of the same article, same paragraph, reads the garbled
+  "KV queue" as an exact KV *sink* and "full compression" as full *density*.)
+* Sol-Engine H3-DataCenter release page, policy paragraph: the first 10 steps
+  and first two layers stay dense; tau = 1.0; no token reordering; an exact
+  951-token multimodal prefix sink; the same online routing on every backend.
+* "Making MiniMax-H3 up to 9x faster on H100s", section "The benchmark was not
+  the product": the sequence is padded to a 64-token multiple and the padding
+  must contribute exactly zero.
+* MiniAcc blog, section "What is Sol attention?": Sol picks promising pairs per
+  head and computes only those.
+
+The pages give no router formula. The reading used here (step numbers follow
+the docstrings below):
+
+1. bf16 -> fp64 (exact).
+2. Blocks are contiguous 64-token ranges; Nb = ceil(S/64); block j has
+   n_j = min(64, S - 64 j) valid tokens.
+3. Pool ("compressed" queries/keys): the arithmetic mean of the valid tokens.
+4. Pooled logits s_ij = scale * qbar_i . kbar_j over all Nb key blocks,
+   scale = 1/sqrt(D) unless given.
+5. p_ij = softmax_j(s_ij).
+6. Keep j iff p_ij >= tau / Nb (at or above tau times the uniform share), OR
+   j is a sink block (64 j < P), OR j == i (the diagonal).
+7. Attention of every query token of block i over the valid tokens of the
+   kept key blocks: exact softmax(scale * q.k) weighted sum of V, and the
+   log-sum-exp of the scaled logits. Non-causal. Padding tokens never enter.
+8. Dense attention = step 7 with every block kept.
+
+The parity of a Sol "correction term" for skipped pairs (MiniAcc blog, same
+section) is not pinned: the pages give no formula and it is not applied.
+"""
+
+from __future__ import annotations
+
+import math
+from typing import Dict, Iterable, List, Optional, Sequence, Tuple
+
+import numpy as np
+
+BLOCK = 64
+TIE_WINDOW = 1e-6
+
+
+def as_f64(x) -> np.ndarray:
+    """Step 1: exact conversion of a bf16 torch tensor (or any array) to fp64."""
+    if hasattr(x, "detach"):  # torch tensor; bf16 -> fp32 -> fp64 is exact
+        x = x.detach().cpu().float().numpy()
+    return np.asarray(x, dtype=np.float64)
+
+
+def num_blocks(S: int, block: int = BLOCK) -> int:
+    return (S + block - 1) // block
+
+
+def block_bounds(S: int, block: int = BLOCK) -> Tuple[np.ndarray, np.ndarray]:
+    """Step 2: start token and valid-token count of each block."""
+    nb = num_blocks(S, block)
+    starts = np.arange(nb, dtype=np.int64) * block
+    counts = np.minimum(block, S - starts)
+    return starts, counts
+
+
+def pool_blocks(x: np.ndarray, block: int = BLOCK) -> np.ndarray:
+    """Step 3: mean over the valid tokens of each block.
+
+    x: [B, S, H, D] fp64. Returns [B, H, Nb, D]. The partial last block is
+    divided by its own token count, not by 64.
+    """
+    B, S, H, D = x.shape
+    starts, counts = block_bounds(S, block)
+    out = np.empty((B, H, len(starts), D), dtype=np.float64)
+    for j, (s0, n) in enumerate(zip(starts, counts)):
+        out[:, :, j, :] = x[:, s0:s0 + n].sum(axis=1) / float(n)
+    return out
+
+
+def pooled_logits(qbar: np.ndarray, kbar: np.ndarray, scale: float) -> np.ndarray:
+    """Step 4: s[b,h,i,j] = scale * qbar[b,h,i] . kbar[b,h,j] (all j)."""
+    return scale * np.matmul(qbar, np.swapaxes(kbar, -1, -2))
+
+
+def pooled_softmax(s: np.ndarray) -> np.ndarray:
+    """Step 5: softmax over the key-block axis, max subtracted first."""
+    m = s.max(axis=-1, keepdims=True)
+    e = np.exp(s - m)
+    return e / e.sum(axis=-1, keepdims=True)
+
+
+def forced_mask(Nb: int, prefix_len: int, block: int = BLOCK) -> np.ndarray:
+    """Step 6, forced part: [Nb, Nb] bool, sink columns and the diagonal.
+
+    Sink blocks are the key blocks that intersect the prefix [0, P), i.e.
+    j < ceil(P/64); every prefix key is then attended with its exact weight.
+    """
+    n_sink = (prefix_len + block - 1) // block
+    f = np.zeros((Nb, Nb), dtype=bool)
+    f[:, :n_sink] = True
+    f[np.arange(Nb), np.arange(Nb)] = True
+    return f
+
+
+def select_blocks(p: np.ndarray, tau: float, prefix_len: int,
+                  block: int = BLOCK) -> np.ndarray:
+    """Step 6: kept[b,h,i,j] = p >= tau/Nb, OR sink, OR diagonal."""
+    Nb = p.shape[-1]
+    kept = p >= (tau / Nb)
+    return kept | forced_mask(Nb, prefix_len, block)
+
+
+def threshold_ratio(p: np.ndarray, tau: float) -> np.ndarray:
+    """p * Nb / tau: a block is kept by the router iff this is >= 1.
+
+    Decisions with |ratio - 1| <= 1e-6 are ties that another correct
+    implementation may take either way.
+    """
+    Nb = p.shape[-1]
+    if tau == 0.0:
+        return np.full_like(p, np.inf)
+    return p * (Nb / tau)
+
+
+def to_csr(kept: np.ndarray) -> Tuple[np.ndarray, np.ndarray]:
+    """Rows (b, h, i) in row-major order; columns ascending."""
+    B, H, Nb, _ = kept.shape
+    flat = kept.reshape(B * H * Nb, Nb)
+    counts = flat.sum(axis=1)
+    row_ptr = np.zeros(B * H * Nb + 1, dtype=np.int64)
+    np.cumsum(counts, out=row_ptr[1:])
+    col_idx = np.nonzero(flat)[1].astype(np.int64)  # row-major scan: ascending per row
+    return row_ptr, col_idx
+
+
+def route_ref(q, k, prefix_len: int, tau: float, scale: Optional[float] = None,
+              block: int = BLOCK) -> Dict[str, np.ndarray]:
+    """Steps 1-6: the block route of every (b, h, query block).
+
+    Returns kept [B,H,Nb,Nb] bool, the CSR (row_ptr, col_idx), the pooled
+    softmax p, the threshold ratio and the forced mask.
+    """
+    qf, kf = as_f64(q), as_f64(k)
+    D = qf.shape[-1]
+    scale = 1.0 / math.sqrt(D) if not scale else scale
+    qbar, kbar = pool_blocks(qf, block), pool_blocks(kf, block)
+    del qf, kf
+    p = pooled_softmax(pooled_logits(qbar, kbar, scale))
+    kept = select_blocks(p, tau, prefix_len, block)
+    row_ptr, col_idx = to_csr(kept)
+    Nb = p.shape[-1]
+    return {"kept": kept, "row_ptr": row_ptr, "col_idx": col_idx, "p": p,
+            "ratio": threshold_ratio(p, tau), "forced": forced_mask(Nb, prefix_len, block),
+            "qbar": qbar, "kbar": kbar}
+
+
+def block_density(kept: np.ndarray) -> float:
+    return float(kept.mean())
+
+
+def attend_rows(qf: np.ndarray, kf: np.ndarray, vf: np.ndarray, b: int, h: int,
+                i: int, blocks: Sequence[int], scale: float,
+                block: int = BLOCK) -> Tuple[np.ndarray, np.ndarray]:
+    """Step 7 for query block i of head h: (O [n_i, D], LSE [n_i]) in fp64.
+
+    The key set is the valid tokens of the listed key blocks, in sequence
+    order; padding tokens (>= S) are never included, so they weigh exactly 0.
+    """
+    S = qf.shape[1]
+    q0, q1 = i * block, min(S, i * block + block)
+    if len(blocks) == 0:
+        # An empty key set: the sum of exponentials is 0, so LSE = log 0 = -inf,
+        # and the output is taken as 0 (an empty weighted sum).
+        return np.zeros((q1 - q0, qf.shape[3])), np.full(q1 - q0, -np.inf)
+    keys = np.concatenate([np.arange(j * block, min(S, j * block + block))
+                           for j in sorted(blocks)])
+    Q = qf[b, q0:q1, h, :]
+    K = kf[b, keys, h, :]
+    V = vf[b, keys, h, :]
+    logits = scale * (Q @ K.T)
+    m = logits.max(axis=1, keepdims=True)
+    e = np.exp(logits - m)
+    z = e.sum(axis=1, keepdims=True)
+    out = (e / z) @ V
+    lse = (m + np.log(z))[:, 0]
+    return out, lse
+
+
+def _head_f64(x, b: int, h: int) -> np.ndarray:
+    """Step 1 for one (batch, head) slice: [S, D] fp64."""
+    if hasattr(x, "detach"):
+        return x[b, :, h, :].detach().cpu().float().numpy().astype(np.float64)
+    return np.asarray(x[b, :, h, :], dtype=np.float64)
+
+
+def attn_ref(q, k, v, row_ptr: np.ndarray, col_idx: np.ndarray,
+             scale: Optional[float] = None,
+             items: Optional[Iterable[Tuple[int, int, int]]] = None,
+             block: int = BLOCK):
+    """Step 7 over a CSR route.
+
+    Without ``items`` it returns the full O [B,S,H,D] and LSE [B,H,S] (fp64).
+    With ``items`` (a list of (b, h, i)) it returns {(b, h, i): (O, LSE)} for
+    just those query blocks.
+    """
+    B, S, H, D = q.shape
+    Nb = num_blocks(S, block)
+    scale = 1.0 / math.sqrt(D) if not scale else scale
+
+    def blocks_of(b, h, i):
+        r = (b * H + h) * Nb + i
+        return [int(c) for c in col_idx[row_ptr[r]:row_ptr[r + 1]]]
+
+    cache = {}
+
+    def head(b, h):
+        if (b, h) not in cache:
+            cache.clear()
+            cache[(b, h)] = tuple(_head_f64(x, b, h)[None, :, None, :] for x in (q, k, v))
+        return cache[(b, h)]
+
+    if items is not None:
+        out = {}
+        for (b, h, i) in sorted(items, key=lambda t: (t[0], t[1], t[2])):
+            qf, kf, vf = head(b, h)
+            out[(b, h, i)] = attend_rows(qf, kf, vf, 0, 0, i, blocks_of(b, h, i), scale, block)
+        return out
+    o = np.zeros((B, S, H, D), dtype=np.float64)
+    lse = np.zeros((B, H, S), dtype=np.float64)
+    for b in range(B):
+        for h in range(H):
+            qf, kf, vf = head(b, h)
+            for i in range(Nb):
+                oi, li = attend_rows(qf, kf, vf, 0, 0, i, blocks_of(b, h, i), scale, block)
+                q0 = i * block
+                o[b, q0:q0 + oi.shape[0], h, :] = oi
+                lse[b, h, q0:q0 + oi.shape[0]] = li
+    return o, lse
+
+
+def dense_csr(B: int, H: int, S: int, block: int = BLOCK) -> Tuple[np.ndarray, np.ndarray]:
+    """Step 8: the route that keeps every key block of every row."""
+    Nb = num_blocks(S, block)
+    return to_csr(np.ones((B, H, Nb, Nb), dtype=bool))
+
+
+def attn_dense_ref(q, k, v, scale: Optional[float] = None,
+                   items: Optional[Iterable[Tuple[int, int, int]]] = None,
+                   block: int = BLOCK):
+    """Step 8: dense attention, i.e. step 7 with every block kept."""
+    B, S, H, _ = q.shape
+    row_ptr, col_idx = dense_csr(B, H, S, block)
+    return attn_ref(q, k, v, row_ptr, col_idx, scale=scale, items=items, block=block)
+
+
+def routed_flops(row_ptr: np.ndarray, col_idx: np.ndarray, B: int, H: int, S: int,
+                 D: int, block: int = BLOCK) -> int:
+    """Algorithmic work of step 7: 4*D*sum over routed (query block, key block)
+    pairs of n_i * n_j (valid tokens only)."""
+    Nb = num_blocks(S, block)
+    _, counts = block_bounds(S, block)
+    rows = np.arange(B * H * Nb)
+    ni = counts[rows % Nb]
+    cs = np.concatenate([[0], np.cumsum(counts[col_idx])])
+    per_row = cs[row_ptr[1:]] - cs[row_ptr[:-1]]
+    return int(4 * D * int((ni * per_row).sum()))
+
+
+def tie_mask(ratio: np.ndarray, forced: np.ndarray) -> np.ndarray:
+    """Decisions another correct router may take either way: router ties
+    (|p Nb / tau - 1| <= 1e-6) on blocks that are not forced."""
+    return (np.abs(ratio - 1.0) <= TIE_WINDOW) & ~forced

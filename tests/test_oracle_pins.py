@@ -1,0 +1,300 @@
+"""Pins of the CPU oracle to things other than itself (no GPU needed).
+
+Each test ties one step of the oracle to a closed form, a hand-worked
+example, a brute-force loop or an invariant, chosen so that a plausible slip
+(a dropped term, a wrong sign or axis, a transposed operand, dividing a
+partial block by 64) fails at least one of them.
+"""
+
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sa_inputs
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def bf16(a):
+    return torch.tensor(np.asarray(a, dtype=np.float32)).to(torch.bfloat16)
+
+
+# ---------------------------------------------------------------- pooling --
+
+def test_pool_ragged_tail_closed_form():
+    # token t of head h, dim d holds t + 100 h + d (all exact in bf16 up to 256)
+    S, H, D = 70, 2, 3
+    x = np.zeros((1, S, H, D))
+    for t in range(S):
+        for h in range(H):
+            for d in range(D):
+                x[0, t, h, d] = t + 100 * h + d
+    pooled = oracle.pool_blocks(x)
+    assert pooled.shape == (1, H, 2, D)
+    for h in range(H):
+        for d in range(D):
+            assert pooled[0, h, 0, d] == 31.5 + 100 * h + d     # mean of 0..63
+            assert pooled[0, h, 1, d] == 66.5 + 100 * h + d     # mean of 64..69 (6 tokens)
+
+
+def test_block_bounds():
+    starts, counts = oracle.block_bounds(38247)
+    assert len(starts) == 598 and counts[-1] == 39 and counts[:-1].min() == 64
+    starts, counts = oracle.block_bounds(64)
+    assert list(counts) == [64]
+    assert oracle.num_blocks(112640) == 1760
+
+
+# ----------------------------------------------------------------- router --
+
+def test_pooled_logits_hand_example():
+    qbar = np.array([[[[1.0, 2.0], [0.0, -1.0]]]])      # [1,1,2,2]
+    kbar = np.array([[[[3.0, 0.5], [-2.0, 4.0], [1.0, 1.0]]]])  # [1,1,3,2]
+    s = oracle.pooled_logits(qbar, kbar, 0.5)
+    want = np.array([[4.0 * 0.5, 6.0 * 0.5, 3.0 * 0.5],
+                     [-0.5 * 0.5, -4.0 * 0.5, -1.0 * 0.5]])
+    np.testing.assert_array_equal(s[0, 0], want)
+
+
+def test_softmax_closed_form():
+    s = np.log(np.array([[1.0, 2.0, 3.0, 6.0]]))
+    p = oracle.pooled_softmax(s)
+    np.testing.assert_allclose(p, [[1 / 12, 2 / 12, 3 / 12, 6 / 12]], rtol=1e-15)
+    # shift invariance of the max-subtracted form, with huge logits
+    p2 = oracle.pooled_softmax(s + 1000.0)
+    np.testing.assert_allclose(p2, p, rtol=1e-13)
+
+
+def _hand_inputs(spec):
+    S, H, D = spec["S"], spec["H"], spec["D"]
+    q = np.zeros((1, S, H, D), np.float32)
+    k = np.zeros((1, S, H, D), np.float32)
+    q[0, :, 0, 0] = 1.0
+    k[0, 64:128, 0, 0] = 0.5
+    k[0, 128:192, 0, 0] = 1.0
+    k[0, 192:196, 0, 0] = 4.0      # block 3: 4 tokens of 4 and 4 of 0 -> mean 2
+    return bf16(q), bf16(k)
+
+
+def test_router_hand_worked_fixture():
+    spec = json.load(open(os.path.join(GOLDEN, "route_hand_example.json")))
+    q, k = _hand_inputs(spec)
+    for case in spec["cases"]:
+        r = oracle.route_ref(q, k, spec["prefix_len"], case["tau"], scale=spec["scale"])
+        rp, ci = r["row_ptr"], r["col_idx"]
+        rows = [list(ci[rp[i]:rp[i + 1]]) for i in range(len(rp) - 1)]
+        assert rows == case["rows"], (case["tau"], rows)
+
+
+def test_threshold_is_inclusive_at_exact_uniform_share():
+    # identical key blocks -> every pooled probability is exactly 1/Nb
+    S, H, D = 256, 1, 4
+    q = bf16(np.random.default_rng(0).standard_normal((1, S, H, D)))
+    k = bf16(np.ones((1, S, H, D)))
+    Nb = 4
+    r = oracle.route_ref(q, k, 0, 1.0)
+    np.testing.assert_array_equal(r["p"], np.full((1, 1, Nb, Nb), 1.0 / Nb))
+    assert r["kept"].all()                                  # p >= tau/Nb with equality
+    assert oracle.route_ref(q, k, 0, 0.999)["kept"].all()
+    only_forced = oracle.route_ref(q, k, 0, 1.001)["kept"][0, 0]
+    np.testing.assert_array_equal(only_forced, np.eye(Nb, dtype=bool))
+
+
+def test_sink_blocks_and_diagonal_are_forced():
+    f = oracle.forced_mask(5, 65)          # P = 65 touches blocks 0 and 1
+    assert f[:, :2].all() and not f[0, 2:].any()
+    assert np.diag(f).all()
+    f0 = oracle.forced_mask(5, 0)          # no prefix: only the diagonal
+    np.testing.assert_array_equal(f0, np.eye(5, dtype=bool))
+    f64 = oracle.forced_mask(5, 64)        # exactly one full block
+    assert f64[:, 0].all() and not f64[0, 1:].any()
+
+
+@pytest.fixture(scope="module")
+def tiny_route():
+    cfg, q, k, v = sa_inputs.make_inputs("tiny")
+    return cfg, q, k, v, oracle.route_ref(q, k, cfg.P, cfg.tau)
+
+
+def test_route_invariants_tiny(tiny_route):
+    cfg, q, k, v, r = tiny_route
+    rp, ci = r["row_ptr"], r["col_idx"]
+    Nb = cfg.Nb
+    n_sink = (cfg.P + 63) // 64
+    for row in range(cfg.H * Nb):
+        cols = ci[rp[row]:rp[row + 1]]
+        assert np.all(np.diff(cols) > 0)                   # sorted, unique
+        i = row % Nb
+        assert i in cols                                    # diagonal
+        assert all(j in cols for j in range(n_sink))        # sink
+    # density the Tiny config is calibrated to
+    assert abs(oracle.block_density(r["kept"]) - 0.25) <= 0.01
+
+
+def test_route_monotone_in_tau(tiny_route):
+    cfg, q, k, v, _ = tiny_route
+    prev = None
+    for tau in (0.0, 0.9, 1.0, 1.01, 1.02, 1.1, 3.0):
+        kept = oracle.route_ref(q, k, cfg.P, tau)["kept"]
+        if prev is not None:
+            assert not (kept & ~prev).any()                # R(tau2) subset of R(tau1)
+        prev = kept
+
+
+def test_tau_zero_keeps_every_block(tiny_route):
+    cfg, q, k, v, _ = tiny_route
+    assert oracle.route_ref(q, k, cfg.P, 0.0)["kept"].all()
+
+
+def test_tau_above_max_keeps_only_forced(tiny_route):
+    cfg, q, k, v, r = tiny_route
+    tau = float(r["p"].max() * cfg.Nb) * 1.0001
+    kept = oracle.route_ref(q, k, cfg.P, tau)["kept"]
+    forced = oracle.forced_mask(cfg.Nb, cfg.P)
+    np.testing.assert_array_equal(kept[0], np.broadcast_to(forced, kept[0].shape))
+
+
+def test_key_block_permutation_permutes_probabilities(tiny_route):
+    cfg, q, k, v, r = tiny_route
+    perm = np.random.default_rng(3).permutation(cfg.Nb)
+    s = oracle.pooled_logits(r["qbar"], r["kbar"][:, :, perm, :], cfg.scale)
+    p_perm = oracle.pooled_softmax(s)
+    np.testing.assert_allclose(p_perm, r["p"][..., perm], rtol=1e-12, atol=0)
+
+
+def test_pooled_route_matches_direct_token_sums():
+    # the pooled logit equals the mean over token pairs of scale * q_t . k_u
+    q, k, _ = sa_inputs.random_small(130, 1, 8, seed=11)
+    r = oracle.route_ref(q, k, 0, 1.0)
+    qf, kf = oracle.as_f64(q), oracle.as_f64(k)
+    scale = 1 / math.sqrt(8)
+    blocks = [(0, 64), (64, 128), (128, 130)]
+    s = np.zeros((3, 3))
+    for i, (a, b) in enumerate(blocks):
+        for j, (c, d) in enumerate(blocks):
+            acc = [scale * float(qf[0, t, 0] @ kf[0, u, 0]) for t in range(a, b) for u in range(c, d)]
+            s[i, j] = math.fsum(acc) / ((b - a) * (d - c))
+    ex = np.exp(s - s.max(axis=1, keepdims=True))
+    np.testing.assert_allclose(r["p"][0, 0], ex / ex.sum(axis=1, keepdims=True), rtol=1e-11)
+
+
+# -------------------------------------------------------------- attention --
+
+def brute_attention(qf, kf, vf, b, h, t, keys, scale):
+    """One query token, pure Python: softmax over the listed key tokens."""
+    logits = [scale * math.fsum(qf[b, t, h, d] * kf[b, u, h, d] for d in range(qf.shape[3]))
+              for u in keys]
+    m = max(logits)
+    w = [math.exp(x - m) for x in logits]
+    z = math.fsum(w)
+    out = [math.fsum(w[n] * vf[b, u, h, d] for n, u in enumerate(keys)) / z
+           for d in range(qf.shape[3])]
+    return out, m + math.log(z)
+
+
+def test_sparse_attention_matches_brute_force_ragged():
+    S, H, D = 150, 2, 4            # blocks of 64, 64, 22 tokens
+    q, k, v = sa_inputs.random_small(S, H, D, seed=5)
+    qf, kf, vf = (oracle.as_f64(x) for x in (q, k, v))
+    # hand-chosen route, rows (h, i): includes an empty-looking off-diagonal mix
+    rows = {(0, 0): [0, 2], (0, 1): [1], (0, 2): [0, 1, 2],
+            (1, 0): [0], (1, 1): [0, 1, 2], (1, 2): [2]}
+    Nb = 3
+    counts = [len(rows[(h, i)]) for h in range(H) for i in range(Nb)]
+    row_ptr = np.concatenate([[0], np.cumsum(counts)])
+    col_idx = np.array([j for h in range(H) for i in range(Nb) for j in rows[(h, i)]])
+    scale = 1 / math.sqrt(D)
+    o, lse = oracle.attn_ref(q, k, v, row_ptr, col_idx)
+    for h in range(H):
+        for i in range(Nb):
+            keys = [u for j in rows[(h, i)] for u in range(64 * j, min(S, 64 * j + 64))]
+            for t in range(64 * i, min(S, 64 * i + 64), 7):
+                want, want_lse = brute_attention(qf, kf, vf, 0, h, t, keys, scale)
+                np.testing.assert_allclose(o[0, t, h], want, rtol=1e-12, atol=1e-14)
+                assert abs(lse[0, h, t] - want_lse) < 1e-12
+
+
+def test_dense_attention_matches_whole_sequence_softmax():
+    q, k, v = sa_inputs.random_small(200, 3, 16, seed=7)
+    qf, kf, vf = (oracle.as_f64(x) for x in (q, k, v))
+    o, lse = oracle.attn_dense_ref(q, k, v)
+    for h in range(3):
+        s = qf[0, :, h] @ kf[0, :, h].T / 4.0
+        m = s.max(axis=1, keepdims=True)
+        e = np.exp(s - m)
+        np.testing.assert_allclose(o[0, :, h], (e / e.sum(1, keepdims=True)) @ vf[0, :, h],
+                                   rtol=1e-11, atol=1e-13)
+        np.testing.assert_allclose(lse[0, h], (m + np.log(e.sum(1, keepdims=True)))[:, 0],
+                                   rtol=1e-13)
+
+
+def test_tau_zero_sparse_equals_dense(tiny_route):
+    cfg, q, k, v, _ = tiny_route
+    r0 = oracle.route_ref(q, k, cfg.P, 0.0)
+    o_s, l_s = oracle.attn_ref(q, k, v, r0["row_ptr"], r0["col_idx"])
+    o_d, l_d = oracle.attn_dense_ref(q, k, v)
+    np.testing.assert_allclose(o_s, o_d, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(l_s, l_d, rtol=0, atol=1e-12)
+
+
+def test_constant_values_give_constant_output():
+    # weights sum to 1 for every row => O == the constant V row
+    q, k, _ = sa_inputs.random_small(100, 2, 8, seed=9)
+    v = torch.full((1, 100, 2, 8), 0.375, dtype=torch.bfloat16)
+    r = oracle.route_ref(q, k, 0, 1.0)
+    o, _ = oracle.attn_ref(q, k, v, r["row_ptr"], r["col_idx"])
+    np.testing.assert_allclose(o, 0.375, rtol=0, atol=1e-14)
+
+
+def test_zero_queries_average_the_valid_keys():
+    # q = 0 => uniform weights over the valid tokens of the kept blocks;
+    # a padded tail that leaked in would shift the mean.
+    S, H, D = 100, 1, 4
+    q = torch.zeros((1, S, H, D), dtype=torch.bfloat16)
+    _, k, v = sa_inputs.random_small(S, H, D, seed=13)
+    o, lse = oracle.attn_dense_ref(q, k, v)
+    vf = oracle.as_f64(v)
+    np.testing.assert_allclose(o[0, 0, 0], vf[0, :, 0].mean(axis=0), rtol=1e-13)
+    np.testing.assert_allclose(lse[0, 0], math.log(S), rtol=1e-15)
+
+
+def test_single_block_sequence_is_dense():
+    q, k, v = sa_inputs.random_small(50, 2, 8, seed=17)
+    r = oracle.route_ref(q, k, 0, 5.0)
+    assert list(r["col_idx"]) == [0, 0]
+    o_s, _ = oracle.attn_ref(q, k, v, r["row_ptr"], r["col_idx"])
+    o_d, _ = oracle.attn_dense_ref(q, k, v)
+    np.testing.assert_array_equal(o_s, o_d)
+
+
+def test_routed_flops_counts_valid_pairs_only():
+    # S = 100: blocks of 64 and 36 tokens; dense route
+    rp, ci = oracle.dense_csr(1, 1, 100)
+    assert oracle.routed_flops(rp, ci, 1, 1, 100, 8) == 4 * 8 * 100 * 100
+    # only the diagonal
+    rp = np.array([0, 1, 2]); ci = np.array([0, 1])
+    assert oracle.routed_flops(rp, ci, 1, 1, 100, 8) == 4 * 8 * (64 * 64 + 36 * 36)
+
+
+def test_tie_mask_window():
+    ratio = np.array([1.0, 1.0 + 5e-7, 1.0 - 2e-6, 0.5])
+    forced = np.array([False, False, False, False])
+    np.testing.assert_array_equal(oracle.tie_mask(ratio, forced), [True, True, False, False])
+
+
+# ------------------------------------------------------------- generators --
+
+def test_generators_shapes_and_determinism():
+    cfg, q, k, v = sa_inputs.make_inputs("tiny")
+    assert q.shape == (1, 1024, 4, 64) and q.dtype == torch.bfloat16
+    _, q2, _, _ = sa_inputs.make_inputs("tiny")
+    assert torch.equal(q, q2)
+    cfg = sa_inputs.get_config("release")
+    assert cfg.P + cfg.grid[0] * cfg.grid[1] * cfg.grid[2] == cfg.S
+    cfg = sa_inputs.get_config("long")
+    assert cfg.S - cfg.P == 110 * 24 * 42 + 809

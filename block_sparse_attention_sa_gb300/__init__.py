@@ -1,0 +1,283 @@
+"""Routed block-sparse self-attention on GB300 (sm_103a): Python binding.
+
+This module only marshals arguments to the C ABI of ``libsa_gb300.so``
+(declared in ``include/sa.h``): it reads tensor pointers, strides and the
+current CUDA stream, allocates outputs with torch when the caller passes
+none, and calls the library. Every step of routing and attention runs in the
+library's CUDA kernels. There is no CPU path: if the library is missing or a
+tensor is not on a CUDA device, the call raises.
+
+Entry points (same names as the C ABI):
+    sa_route(q, k, prefix_len, tau, ...)              -> (row_ptr, col_idx)
+    sa_attn_sparse(q, k, v, row_ptr, col_idx, ...)    -> (o, lse)
+    sa_attn_dense(q, k, v, ...)                       -> (o, lse)
+    sa_forward_host(q_host, k_host, v_host, ...)      -> o_host (+ lse_host)
+Tensors are [B, S, H, D] bf16 with a contiguous last dimension.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Tuple
+
+import torch
+
+__all__ = [
+    "SaError", "load_library", "library_path", "sa_params", "make_params", "sa_route",
+    "sa_attn_sparse", "sa_attn_dense", "sa_forward_host", "sa_route_workspace_bytes",
+    "sa_attn_workspace_bytes", "sa_route_max_nnz", "check_dev_status", "EXPORTS",
+    "SA_DEV_CAPACITY", "SA_DEV_TIMEOUT", "SA_DEV_BAD_ROUTE", "SA_DEV_RANGE",
+]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB = None
+
+SA_OK, SA_ERR_INVALID_ARG, SA_ERR_UNSUPPORTED, SA_ERR_CAPACITY, SA_ERR_CUDA, SA_ERR_TIMEOUT = range(6)
+SA_DEV_CAPACITY, SA_DEV_TIMEOUT, SA_DEV_BAD_ROUTE, SA_DEV_RANGE = 1, 2, 4, 8
+
+# Every function include/sa.h declares.
+EXPORTS = (
+    "sa_params_init", "sa_num_blocks", "sa_route_rows", "sa_route_max_nnz",
+    "sa_route_workspace_bytes", "sa_route", "sa_attn_workspace_bytes", "sa_attn_sparse",
+    "sa_attn_dense", "sa_forward_host", "sa_dev_status_decode", "sa_status_string",
+)
+
+
+class SaError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what}: {_status_name(code)}")
+
+
+class sa_params(ctypes.Structure):
+    _fields_ = [
+        ("B", ctypes.c_int32), ("S", ctypes.c_int32), ("H", ctypes.c_int32), ("D", ctypes.c_int32),
+        ("block", ctypes.c_int32), ("prefix_len", ctypes.c_int32),
+        ("tau", ctypes.c_float), ("softmax_scale", ctypes.c_float),
+        ("q_stride", ctypes.c_int64 * 3), ("k_stride", ctypes.c_int64 * 3),
+        ("v_stride", ctypes.c_int64 * 3), ("o_stride", ctypes.c_int64 * 3),
+    ]
+
+
+def library_path() -> str:
+    return os.path.join(_PKG, "libsa_gb300.so")
+
+
+def load_library(path: Optional[str] = None) -> ctypes.CDLL:
+    """Load (once) and type the shared library. Raises if it is missing."""
+    global _LIB
+    if _LIB is not None and path is None:
+        return _LIB
+    p = path or library_path()
+    if not os.path.exists(p):
+        raise FileNotFoundError(
+            f"{p} is missing: build it with `python -m block_sparse_attention_sa_gb300.build`")
+    lib = ctypes.CDLL(p)
+    P = ctypes.POINTER(sa_params)
+    vp, i32p, i64, sz = ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32), ctypes.c_int64, ctypes.c_size_t
+    sig = {
+        "sa_params_init": (None, [P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                  ctypes.c_int32, ctypes.c_float]),
+        "sa_num_blocks": (ctypes.c_int32, [P]),
+        "sa_route_rows": (i64, [P]),
+        "sa_route_max_nnz": (i64, [P]),
+        "sa_route_workspace_bytes": (sz, [P]),
+        "sa_attn_workspace_bytes": (sz, [P]),
+        "sa_route": (ctypes.c_int, [P, vp, vp, vp, vp, i64, vp, sz, vp, vp]),
+        "sa_attn_sparse": (ctypes.c_int, [P, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp]),
+        "sa_attn_dense": (ctypes.c_int, [P, vp, vp, vp, vp, vp, vp, sz, vp, vp]),
+        "sa_forward_host": (ctypes.c_int, [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i64,
+                                           vp, sz, vp, vp]),
+        "sa_dev_status_decode": (ctypes.c_int, [ctypes.c_int32]),
+        "sa_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    if path is None:
+        _LIB = lib
+    return lib
+
+
+def _status_name(code: int) -> str:
+    try:
+        return load_library().sa_status_string(code).decode()
+    except Exception:  # library not loadable: still report the number
+        return f"status {code}"
+
+
+def _check(code: int, what: str) -> None:
+    if code != SA_OK:
+        raise SaError(code, what)
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _bshd_strides(t: torch.Tensor, name: str):
+    if t.dim() != 4 or t.stride(3) != 1:
+        raise ValueError(f"{name} must be [B, S, H, D] with a contiguous last dimension")
+    return (t.stride(0), t.stride(1), t.stride(2))
+
+
+def _require_cuda(*ts):
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise ValueError("tensors must be on a CUDA device: there is no CPU path")
+
+
+def make_params(q: torch.Tensor, k: Optional[torch.Tensor] = None, v: Optional[torch.Tensor] = None,
+                o: Optional[torch.Tensor] = None, prefix_len: int = 0, tau: float = 1.0,
+                scale: float = 0.0) -> sa_params:
+    B, S, H, D = q.shape
+    p = sa_params()
+    p.B, p.S, p.H, p.D, p.block = B, S, H, D, 64
+    p.prefix_len, p.tau, p.softmax_scale = int(prefix_len), float(tau), float(scale)
+    for field, t in (("q_stride", q), ("k_stride", k if k is not None else q),
+                     ("v_stride", v if v is not None else q), ("o_stride", o if o is not None else q)):
+        st = _bshd_strides(t, field[0])
+        arr = getattr(p, field)
+        for i in range(3):
+            arr[i] = st[i]
+    return p
+
+
+def sa_route_workspace_bytes(p: sa_params) -> int:
+    return int(load_library().sa_route_workspace_bytes(ctypes.byref(p)))
+
+
+def sa_attn_workspace_bytes(p: sa_params) -> int:
+    return int(load_library().sa_attn_workspace_bytes(ctypes.byref(p)))
+
+
+def sa_route_max_nnz(p: sa_params) -> int:
+    return int(load_library().sa_route_max_nnz(ctypes.byref(p)))
+
+
+def _workspace(nbytes: int, device, ws: Optional[torch.Tensor]) -> torch.Tensor:
+    if ws is not None:
+        if ws.numel() * ws.element_size() < nbytes:
+            raise ValueError("workspace too small")
+        return ws
+    return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+
+
+def sa_route(q: torch.Tensor, k: torch.Tensor, prefix_len: int, tau: float, scale: float = 0.0, *,
+             row_ptr: Optional[torch.Tensor] = None, col_idx: Optional[torch.Tensor] = None,
+             workspace: Optional[torch.Tensor] = None, dev_status: Optional[torch.Tensor] = None,
+             stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Block route of every (b, h, query block): int32 row_ptr [B*H*Nb+1] and
+    col_idx (capacity B*H*Nb*Nb unless given; valid entries are
+    col_idx[:row_ptr[-1]])."""
+    _require_cuda(q, k)
+    lib = load_library()
+    p = make_params(q, k, prefix_len=prefix_len, tau=tau, scale=scale)
+    rows = int(lib.sa_route_rows(ctypes.byref(p)))
+    if rows == 0:
+        _check(SA_ERR_INVALID_ARG, "sa_route")
+    if row_ptr is None:
+        row_ptr = torch.empty(rows + 1, dtype=torch.int32, device=q.device)
+    if col_idx is None:
+        col_idx = torch.empty(sa_route_max_nnz(p), dtype=torch.int32, device=q.device)
+    ws = _workspace(sa_route_workspace_bytes(p), q.device, workspace)
+    code = lib.sa_route(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(row_ptr), _ptr(col_idx),
+                        col_idx.numel(), _ptr(ws), ws.numel() * ws.element_size(),
+                        _ptr(dev_status), _stream(stream))
+    _check(code, "sa_route")
+    return row_ptr, col_idx
+
+
+def _attn_out(q, o, lse, want_lse):
+    B, S, H, D = q.shape
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((B, H, S), dtype=torch.float32, device=q.device)
+    return o, lse
+
+
+def sa_attn_sparse(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, row_ptr: torch.Tensor,
+                   col_idx: torch.Tensor, scale: float = 0.0, *, o: Optional[torch.Tensor] = None,
+                   lse: Optional[torch.Tensor] = None, want_lse: bool = True,
+                   workspace: Optional[torch.Tensor] = None,
+                   dev_status: Optional[torch.Tensor] = None, stream=None):
+    """Attention over the routed key blocks: (o bf16 [B,S,H,D], lse fp32 [B,H,S] or None)."""
+    _require_cuda(q, k, v, row_ptr, col_idx)
+    lib = load_library()
+    o, lse = _attn_out(q, o, lse, want_lse)
+    p = make_params(q, k, v, o, scale=scale)
+    ws = _workspace(sa_attn_workspace_bytes(p), q.device, workspace)
+    code = lib.sa_attn_sparse(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(row_ptr),
+                              _ptr(col_idx), _ptr(o), _ptr(lse), _ptr(ws),
+                              ws.numel() * ws.element_size(), _ptr(dev_status), _stream(stream))
+    _check(code, "sa_attn_sparse")
+    return o, lse
+
+
+def sa_attn_dense(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float = 0.0, *,
+                  o: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                  want_lse: bool = True, workspace: Optional[torch.Tensor] = None,
+                  dev_status: Optional[torch.Tensor] = None, stream=None):
+    """Attention over every key block (density 100%)."""
+    _require_cuda(q, k, v)
+    lib = load_library()
+    o, lse = _attn_out(q, o, lse, want_lse)
+    p = make_params(q, k, v, o, scale=scale)
+    ws = _workspace(sa_attn_workspace_bytes(p), q.device, workspace)
+    code = lib.sa_attn_dense(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                             _ptr(ws), ws.numel() * ws.element_size(), _ptr(dev_status),
+                             _stream(stream))
+    _check(code, "sa_attn_dense")
+    return o, lse
+
+
+def sa_forward_host(q_host: torch.Tensor, k_host: torch.Tensor, v_host: torch.Tensor,
+                    prefix_len: int, tau: float, scale: float = 0.0, *, bufs: dict,
+                    o_host: Optional[torch.Tensor] = None, lse_host: Optional[torch.Tensor] = None,
+                    stream=None) -> torch.Tensor:
+    """One layer from (pinned) host tensors through the device buffers in
+    ``bufs`` (q, k, v, o, lse, row_ptr, col_idx, ws, status); returns o_host.
+    Enqueues only; synchronise the stream before reading o_host."""
+    lib = load_library()
+    if o_host is None:
+        o_host = torch.empty_like(q_host, pin_memory=True)
+    p = make_params(bufs["q"], prefix_len=prefix_len, tau=tau, scale=scale)
+    ws = bufs["ws"]
+    code = lib.sa_forward_host(
+        ctypes.byref(p), _ptr(q_host), _ptr(k_host), _ptr(v_host), _ptr(o_host), _ptr(lse_host),
+        _ptr(bufs["q"]), _ptr(bufs["k"]), _ptr(bufs["v"]), _ptr(bufs["o"]), _ptr(bufs.get("lse")),
+        _ptr(bufs["row_ptr"]), _ptr(bufs["col_idx"]), bufs["col_idx"].numel(), _ptr(ws),
+        ws.numel() * ws.element_size(), _ptr(bufs.get("status")), _stream(stream))
+    _check(code, "sa_forward_host")
+    return o_host
+
+
+def alloc_layer_buffers(B: int, S: int, H: int, D: int, device="cuda") -> dict:
+    """Device buffers for sa_forward_host (one workspace sized for both calls)."""
+    q = torch.empty((B, S, H, D), dtype=torch.bfloat16, device=device)
+    p = make_params(q)
+    bufs = {"q": q, "k": torch.empty_like(q), "v": torch.empty_like(q), "o": torch.empty_like(q),
+            "lse": torch.empty((B, H, S), dtype=torch.float32, device=device),
+            "row_ptr": torch.empty(int(load_library().sa_route_rows(ctypes.byref(p))) + 1,
+                                   dtype=torch.int32, device=device),
+            "col_idx": torch.empty(sa_route_max_nnz(p), dtype=torch.int32, device=device),
+            "status": torch.zeros(1, dtype=torch.int32, device=device)}
+    nbytes = max(sa_route_workspace_bytes(p), sa_attn_workspace_bytes(p))
+    bufs["ws"] = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    return bufs
+
+
+def check_dev_status(dev_status: torch.Tensor, what: str = "device status") -> None:
+    """Raise if the kernels reported a device-side condition."""
+    val = int(dev_status.item())
+    if val:
+        raise SaError(int(load_library().sa_dev_status_decode(val)), f"{what} (bits {val:#x})")

@@ -1,0 +1,520 @@
+// attn.cu -- block-sparse flash-attention forward on sm_103a (tcgen05/TMEM/TMA).
+//
+// What is computed: for every query token of 64-token block i, exact softmax
+// attention over the valid tokens of the key blocks routed to (b, h, i)
+// (MiniAcc blog, "What is Sol attention?": only the selected pairs are
+// computed; "MiniMax H3 runs on single 4090 with 4.44x speedup over dense
+// execution", third paragraph: the exact prefix sink and the diagonal are
+// part of every route). Dense mode lists every key block.
+//
+// Tile and roles. One CTA owns a 128-row query tile = query blocks 2p and
+// 2p+1 of one head (tcgen05 M = 128; the route is per 64-row block). It
+// walks the ascending union of the two blocks' key lists, two 64-key blocks
+// per step (N = 128); a key block listed for only one of the two query
+// blocks is masked to -inf for the other half's rows, so each row still sees
+// exactly its own key set. Six warps:
+//   warps 0-3  softmax + epilogue, one thread per query row (TMEM lane)
+//   warp  4    builds the tile's key-block union in shared memory, then one
+//              lane issues every TMA load (Q once; K and V^T per step)
+//   warp  5    allocates TMEM; one lane issues every tcgen05.mma
+// Pipeline per step j: K(j) -> S[j%2] = Q K^T (bf16, fp32 in TMEM)
+//   -> softmax(j) reads S, writes P (fp16) to shared memory, rescales O
+//   in TMEM when the running max moved by more than 2^8
+//   -> O += P V (fp16, fp32 in TMEM). QK^T(j+1) overlaps softmax(j).
+// The producer alone reads the route, before the pipeline starts, so no
+// data-dependent load sits inside the pipelined loops.
+// Every wait is bounded (SA_DEV_TIMEOUT) and an aborted CTA drains its own
+// copies and MMAs and frees TMEM before it exits.
+#include <cmath>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "ptx.cuh"
+#include "sa_internal.cuh"
+
+namespace sa {
+
+namespace {
+
+constexpr int BM = 128;   // query rows per tile
+constexpr int BN = 128;   // key rows per step (two key blocks)
+constexpr int KST = 2;    // K stages
+constexpr int VST = 2;    // V stages
+constexpr int kThreads = 192;
+constexpr int kTmemCols = 512;
+constexpr int kColS0 = 0, kColS1 = 128, kColO = 256;
+constexpr float kRescaleLog2 = 8.0f;  // lazy-rescale threshold: P <= 2^8 in fp16
+
+template <int D>
+struct Smem {
+  static constexpr int kRegion = BM * 128;            // one 64-wide K slice of 128 rows
+  static constexpr int kQ = 0;
+  static constexpr int kQBytes = BM * D * 2;
+  static constexpr int kK = kQ + kQBytes;
+  static constexpr int kKBytes = BN * D * 2;
+  static constexpr int kV = kK + KST * kKBytes;
+  static constexpr int kVBytes = BN * D * 2;
+  static constexpr int kVHalf = D * 128;              // one 64-key half of a V^T stage
+  static constexpr int kP = kV + VST * kVBytes;
+  static constexpr int kPBytes = BM * BN * 2;
+  static constexpr int kBar = kP + kPBytes;
+  // barriers
+  static constexpr int bQFull = 0;
+  static constexpr int bKFull = 1;
+  static constexpr int bKEmpty = bKFull + KST;
+  static constexpr int bVFull = bKEmpty + KST;
+  static constexpr int bVEmpty = bVFull + VST;
+  static constexpr int bSFull = bVEmpty + VST;
+  static constexpr int bPFull = bSFull + 2;
+  static constexpr int bOReady = bPFull + 1;
+  static constexpr int bFin = bOReady + 1;
+  static constexpr int kNumBars = bFin + 1;
+  static constexpr int kMisc = kBar + kNumBars * 8;   // tmem base, abort, n_entries
+  static constexpr int kBits = kMisc + 64;
+  static constexpr int kInfo = kBits + 2 * (kMaxNbAttn / 32) * 4;
+  static constexpr int kEnd = kInfo + kMaxNbAttn * 2;
+  static constexpr int kBytes = kEnd + 1024;          // slack to align the base to 1 KB
+};
+
+__device__ __forceinline__ uint32_t pack_half2(float a, float b) {
+  const __half2 h = __floats2half2_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+__device__ __forceinline__ uint32_t pack_bf162(float a, float b) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+__device__ __forceinline__ void set_status(int32_t* st, int bits) {
+  if (st) atomicOr(st, bits);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                const __grid_constant__ CUtensorMap tm_vt, const AttnArgs a) {
+  using L = Smem<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int pair = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int Nb = a.Nb, S = a.S;
+  const int qb0 = 2 * pair;
+  const bool has_qb1 = qb0 + 1 < Nb;
+
+  uint32_t* misc = reinterpret_cast<uint32_t*>(smem + L::kMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
+  const AbortSignal abort_sig{abort_flag, a.dev_status};
+  const volatile int never_flag = 0;
+  const AbortSignal drain_sig{&never_flag, nullptr};  // drains wait out their own limit
+  uint32_t* bmA = reinterpret_cast<uint32_t*>(smem + L::kBits);
+  uint32_t* bmB = bmA + kMaxNbAttn / 32;
+  uint16_t* info = reinterpret_cast<uint16_t*>(smem + L::kInfo);
+  auto bar = [&](int i) { return sbase + L::kBar + 8u * static_cast<uint32_t>(i); };
+
+  // ---------------------------------------------------------------- setup
+  if (threadIdx.x == 0) {
+    // p_full: every softmax thread arrives; the rest: one arrival (TMA
+    // expect_tx or tcgen05.commit).
+    for (int i = 0; i < L::kNumBars; ++i) mbar_init(bar(i), i == L::bPFull ? BM : 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(sbase + L::kMisc, kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == 4) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_vt);
+    }
+    // Union of the two query blocks' key lists, ascending, with a 2-bit
+    // membership mask per key block: bit 0 = block 2p lists it, bit 1 = 2p+1.
+    const int words = (Nb + 31) >> 5;
+    int bad = 0;
+    if (a.row_ptr == nullptr) {
+      const uint16_t m = has_qb1 ? 3 : 1;
+      for (int j = lane; j < Nb; j += 32) info[j] = static_cast<uint16_t>((j << 2) | m);
+      if (lane == 0) misc[2] = static_cast<uint32_t>(Nb);
+    } else {
+      for (int w = lane; w < words; w += 32) { bmA[w] = 0u; bmB[w] = 0u; }
+      __syncwarp();
+      for (int half = 0; half < 2; ++half) {
+        if (half == 1 && !has_qb1) break;
+        const int64_t r = (static_cast<int64_t>(b) * a.H + h) * Nb + qb0 + half;
+        const int beg = a.row_ptr[r], end = a.row_ptr[r + 1];
+        if (beg < 0 || end < beg || end - beg > Nb) { bad = 1; continue; }
+        uint32_t* bm = half ? bmB : bmA;
+        for (int e = beg + lane; e < end; e += 32) {
+          const int j = a.col_idx[e];
+          if (j < 0 || j >= Nb) bad = 1;
+          else atomicOr(&bm[j >> 5], 1u << (j & 31));
+        }
+      }
+      __syncwarp();
+      int total = 0;
+      for (int w0 = 0; w0 < words; w0 += 32) {
+        const int w = w0 + lane;
+        const uint32_t ua = w < words ? bmA[w] : 0u, ub = w < words ? bmB[w] : 0u;
+        uint32_t u = ua | ub;
+        const int c = __popc(u);
+        int incl = c;
+        for (int off = 1; off < 32; off <<= 1) {
+          const int v = __shfl_up_sync(0xffffffffu, incl, off);
+          if (lane >= off) incl += v;
+        }
+        int pos = total + incl - c;
+        while (u) {
+          const int bit = __ffs(u) - 1;
+          const uint32_t m = ((ua >> bit) & 1u) | (((ub >> bit) & 1u) << 1);
+          info[pos++] = static_cast<uint16_t>(((w * 32 + bit) << 2) | m);
+          u &= u - 1;
+        }
+        total += __shfl_sync(0xffffffffu, incl, 31);
+      }
+      if (lane == 0) misc[2] = static_cast<uint32_t>(total);
+    }
+    if (__any_sync(0xffffffffu, bad) && lane == 0) set_status(a.dev_status, SA_DEV_BAD_ROUTE);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = misc[0];
+  const int n_entries = static_cast<int>(misc[2]);
+  const int n_steps = (n_entries + 1) >> 1;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int k_issued[KST] = {0}, v_issued[VST] = {0};
+      bool ok = true;
+      mbar_arrive_expect_tx(bar(L::bQFull), L::kQBytes);
+      for (int qh = 0; qh < 2; ++qh)
+        for (int dh = 0; dh < D / 64; ++dh)
+          tma_load_4d(sbase + L::kQ + dh * L::kRegion + qh * 8192, &tm_q, bar(L::bQFull),
+                      dh * 64, (qb0 + qh) * kBlock, h, b);
+      for (int j = 0; j < n_steps && ok; ++j) {
+        const int nblk = (2 * j + 1 < n_entries) ? 2 : 1;
+        const int ks = j % KST;
+        if (j >= KST) ok = mbar_wait(bar(L::bKEmpty + ks), ((j / KST) - 1) & 1, abort_sig);
+        if (!ok) break;
+        mbar_arrive_expect_tx(bar(L::bKFull + ks), nblk * kBlock * D * 2);
+        ++k_issued[ks];
+        for (int kh = 0; kh < nblk; ++kh) {
+          const int jk = info[2 * j + kh] >> 2;
+          for (int dh = 0; dh < D / 64; ++dh)
+            tma_load_4d(sbase + L::kK + ks * L::kKBytes + dh * L::kRegion + kh * 8192, &tm_k,
+                        bar(L::bKFull + ks), dh * 64, jk * kBlock, h, b);
+        }
+        const int vs = j % VST;
+        if (j >= VST) ok = mbar_wait(bar(L::bVEmpty + vs), ((j / VST) - 1) & 1, abort_sig);
+        if (!ok) break;
+        mbar_arrive_expect_tx(bar(L::bVFull + vs), nblk * kBlock * D * 2);
+        ++v_issued[vs];
+        for (int kh = 0; kh < nblk; ++kh) {
+          const int jk = info[2 * j + kh] >> 2;
+          tma_load_3d(sbase + L::kV + vs * L::kVBytes + kh * L::kVHalf, &tm_vt,
+                      bar(L::bVFull + vs), jk * kBlock, 0, b * a.H + h);
+        }
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        set_status(a.dev_status, SA_DEV_TIMEOUT);
+      }
+      if (*abort_flag) {
+        // Drain: every copy this CTA started lands before shared memory goes away.
+        mbar_wait(bar(L::bQFull), 0, drain_sig);
+        for (int s = 0; s < KST; ++s)
+          if (k_issued[s]) mbar_wait(bar(L::bKFull + s), (k_issued[s] - 1) & 1, drain_sig);
+        for (int s = 0; s < VST; ++s)
+          if (v_issued[s]) mbar_wait(bar(L::bVFull + s), (v_issued[s] - 1) & 1, drain_sig);
+      }
+    }
+  } else if (warp == 5) {
+    // ----------------------------------------------------------------- MMA
+    if (lane == 0) {
+      constexpr uint32_t kIdQK128 = idesc_f16(BM, 128, 1);
+      constexpr uint32_t kIdQK64 = idesc_f16(BM, 64, 1);
+      constexpr uint32_t kIdPV = idesc_f16(BM, D, 0);
+      // Q always lands before the CTA can exit, even with an empty route.
+      bool ok = mbar_wait(bar(L::bQFull), 0, abort_sig);
+      auto issue_qk = [&](int j) -> bool {
+        const int ks = j % KST;
+        if (!mbar_wait(bar(L::bKFull + ks), (j / KST) & 1, abort_sig)) return false;
+        tc_fence_after();
+        const int nblk = (2 * j + 1 < n_entries) ? 2 : 1;
+        const uint32_t d_tmem = tmem + ((j & 1) ? kColS1 : kColS0);
+        const uint32_t qa = sbase + L::kQ, kb = sbase + L::kK + ks * L::kKBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * L::kRegion + (kk & 3) * 32;
+          umma_ss(d_tmem, sdesc_kmajor_sw128(qa + off), sdesc_kmajor_sw128(kb + off),
+                  nblk == 2 ? kIdQK128 : kIdQK64, kk > 0);
+        }
+        umma_commit(bar(L::bSFull + (j & 1)));
+        umma_commit(bar(L::bKEmpty + ks));
+        return true;
+      };
+      if (ok && n_steps > 0) {
+        tc_fence_after();
+        ok = issue_qk(0);
+      }
+      for (int j = 0; j < n_steps && ok; ++j) {
+        if (j + 1 < n_steps && !issue_qk(j + 1)) { ok = false; break; }
+        if (!mbar_wait(bar(L::bPFull), j & 1, abort_sig)) { ok = false; break; }
+        tc_fence_after();
+        const int vs = j % VST;
+        if (!mbar_wait(bar(L::bVFull + vs), (j / VST) & 1, abort_sig)) { ok = false; break; }
+        tc_fence_after();
+        const int nblk = (2 * j + 1 < n_entries) ? 2 : 1;
+        const uint32_t pa = sbase + L::kP, vb = sbase + L::kV + vs * L::kVBytes;
+        for (int kk = 0; kk < nblk * 4; ++kk) {
+          const uint32_t kh = kk >> 2, off = (kk & 3) * 32;
+          umma_ss(tmem + kColO, sdesc_kmajor_sw128(pa + kh * L::kRegion + off),
+                  sdesc_kmajor_sw128(vb + kh * L::kVHalf + off), kIdPV, (j > 0 || kk > 0));
+        }
+        umma_commit(bar(L::bOReady));
+        umma_commit(bar(L::bVEmpty + vs));
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        set_status(a.dev_status, SA_DEV_TIMEOUT);
+      }
+      // Every MMA issued above completes before TMEM is released.
+      umma_commit(bar(L::bFin));
+      mbar_wait(bar(L::bFin), 0, drain_sig);
+    }
+  } else {
+    // ------------------------------------------------------------- softmax
+    const int r = threadIdx.x;                 // tile row == TMEM lane
+    const int qh = r >> 6;
+    const int t = qb0 * kBlock + r;            // query token
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const int last_valid = S - (Nb - 1) * kBlock;  // tokens in the last block
+    float m_run = -INFINITY, l_run = 0.f;
+    bool ok = true;
+
+    for (int j = 0; j < n_steps; ++j) {
+      if (!mbar_wait_warp(bar(L::bSFull + (j & 1)), (j >> 1) & 1, abort_sig)) { ok = false; break; }
+      tc_fence_after();
+      const int nblk = (2 * j + 1 < n_entries) ? 2 : 1;
+      const uint32_t e0 = info[2 * j];
+      const uint32_t e1 = nblk == 2 ? info[2 * j + 1] : 0u;
+      const uint32_t s_col = (j & 1) ? kColS1 : kColS0;
+
+      float x[BN];
+      {
+        uint32_t raw[32];
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          tmem_ld32(lane_base + s_col + 32 * c, raw);
+          tmem_wait_ld();
+#pragma unroll
+          for (int u = 0; u < 32; ++u) x[32 * c + u] = __uint_as_float(raw[u]);
+        }
+        if (nblk == 2) {
+#pragma unroll
+          for (int c = 2; c < 4; ++c) {
+            tmem_ld32(lane_base + s_col + 32 * c, raw);
+            tmem_wait_ld();
+#pragma unroll
+            for (int u = 0; u < 32; ++u) x[32 * c + u] = __uint_as_float(raw[u]);
+          }
+        }
+      }
+      // masks: membership of this row's query block, and the ragged tail
+      int nv[2];
+      {
+        const uint32_t ee[2] = {e0, e1};
+#pragma unroll
+        for (int kh = 0; kh < 2; ++kh) {
+          const int jk = static_cast<int>(ee[kh] >> 2);
+          const bool member = kh < nblk && ((ee[kh] >> qh) & 1u);
+          nv[kh] = member ? (jk == Nb - 1 ? last_valid : kBlock) : 0;
+        }
+      }
+      float bmax = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < BN; ++c) {
+        const int kh = c >> 6, cc = c & 63;
+        x[c] = (cc < nv[kh]) ? x[c] * a.scale_log2 : -INFINITY;
+        bmax = fmaxf(bmax, x[c]);
+      }
+      float m_new = m_run;
+      if (bmax > m_run + kRescaleLog2 || (m_run == -INFINITY && bmax > -INFINITY)) m_new = bmax;
+      const float alpha = (m_new == m_run) ? 1.f : exp2f(m_run - m_new);
+      float rsum = 0.f;
+      uint32_t pk[BN / 2];
+#pragma unroll
+      for (int c = 0; c < BN; c += 2) {
+        const float p0 = (x[c] == -INFINITY) ? 0.f : exp2f(x[c] - m_new);
+        const float p1 = (x[c + 1] == -INFINITY) ? 0.f : exp2f(x[c + 1] - m_new);
+        rsum += p0 + p1;
+        pk[c >> 1] = pack_half2(p0, p1);
+      }
+      l_run = l_run * alpha + rsum;
+      m_run = m_new;
+
+      if (j > 0) {
+        // PV(j-1) done: O is stable and the P buffer is free.
+        if (!mbar_wait_warp(bar(L::bOReady), (j - 1) & 1, abort_sig)) { ok = false; break; }
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+          uint32_t o[32];
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            tmem_ld32(lane_base + kColO + 32 * c, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int u = 0; u < 32; ++u) o[u] = __float_as_uint(__uint_as_float(o[u]) * alpha);
+            tmem_st32(lane_base + kColO + 32 * c, o);
+          }
+          tmem_wait_st();
+        }
+      }
+      // P row -> shared memory, K-major, 128-byte swizzle (chunk ^ row%8).
+      {
+        uint8_t* prow = smem + L::kP + r * 128;
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          if (c >= 8 && nblk == 1) break;
+          const int kh = c >> 3, ch = c & 7;
+          uint4 v = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+          *reinterpret_cast<uint4*>(prow + kh * L::kRegion + ((ch ^ (r & 7)) << 4)) = v;
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(bar(L::bPFull));
+    }
+    if (!ok) {
+      *abort_flag = 1;
+      set_status(a.dev_status, SA_DEV_TIMEOUT);
+    }
+
+    // ------------------------------------------------------------ epilogue
+    bool have_o = ok && n_steps > 0;
+    if (have_o) {
+      have_o = mbar_wait_warp(bar(L::bOReady), (n_steps - 1) & 1, abort_sig);
+      if (!have_o) {
+        *abort_flag = 1;
+        set_status(a.dev_status, SA_DEV_TIMEOUT);
+      }
+      tc_fence_after();
+    }
+    const bool row_ok = t < S;
+    const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
+    uint16_t* orow = a.o + b * a.os[0] + static_cast<int64_t>(t) * a.os[1] + h * a.os[2];
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) {
+      uint32_t o[32];
+      if (have_o) {
+        tmem_ld32(lane_base + kColO + 32 * c, o);
+        tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int u = 0; u < 32; ++u) o[u] = 0u;
+      }
+      if (row_ok) {
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          uint4 w;
+          w.x = pack_bf162(__uint_as_float(o[8 * v + 0]) * inv_l, __uint_as_float(o[8 * v + 1]) * inv_l);
+          w.y = pack_bf162(__uint_as_float(o[8 * v + 2]) * inv_l, __uint_as_float(o[8 * v + 3]) * inv_l);
+          w.z = pack_bf162(__uint_as_float(o[8 * v + 4]) * inv_l, __uint_as_float(o[8 * v + 5]) * inv_l);
+          w.w = pack_bf162(__uint_as_float(o[8 * v + 6]) * inv_l, __uint_as_float(o[8 * v + 7]) * inv_l);
+          *reinterpret_cast<uint4*>(orow + 32 * c + 8 * v) = w;
+        }
+      }
+    }
+    if (row_ok && a.lse) {
+      const float lse = l_run > 0.f ? m_run * 0.69314718055994531f + logf(l_run) : -INFINITY;
+      a.lse[(static_cast<int64_t>(b) * a.H + h) * S + t] = lse;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 5) tmem_dealloc(tmem, kTmemCols);
+}
+
+// V [B,S,H,D] bf16 -> vt [B*H][D][s_pad] fp16. grid (ceil(S/64), H, B), 256 threads.
+template <int D>
+__global__ void __launch_bounds__(256)
+pack_v_kernel(const uint16_t* __restrict__ v, int64_t vs0, int64_t vs1, int64_t vs2, int S, int H,
+              int s_pad, uint16_t* __restrict__ vt, int32_t* dev_status) {
+  __shared__ uint16_t tile[kBlock][D + 8];
+  const int s0 = blockIdx.x * kBlock, h = blockIdx.y, b = blockIdx.z;
+  bool range = false;
+  constexpr int VPR = D / 8;  // 16-byte vectors per token row
+  for (int idx = threadIdx.x; idx < kBlock * VPR; idx += 256) {
+    const int r = idx / VPR, c = (idx % VPR) * 8;
+    uint4 w = make_uint4(0, 0, 0, 0);
+    if (s0 + r < S)
+      w = __ldg(reinterpret_cast<const uint4*>(v + b * vs0 + static_cast<int64_t>(s0 + r) * vs1 +
+                                               h * vs2 + c));
+    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const float f = __uint_as_float((hh ? (ww[u] & 0xffff0000u) : (ww[u] << 16)));
+        const __half hv = __float2half_rn(f);
+        if (isinf(__half2float(hv)) && !isinf(f)) range = true;
+        tile[r][c + 2 * u + hh] = *reinterpret_cast<const uint16_t*>(&hv);
+      }
+    }
+  }
+  __syncthreads();
+  uint16_t* dst = vt + (static_cast<int64_t>(b) * H + h) * D * s_pad;
+  for (int idx = threadIdx.x; idx < D * (kBlock / 8); idx += 256) {
+    const int d = idx / (kBlock / 8), c = (idx % (kBlock / 8)) * 8;
+    if (s0 + c >= s_pad) continue;
+    uint16_t e[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) e[u] = tile[c + u][d];
+    uint4 w;
+    w.x = e[0] | (static_cast<uint32_t>(e[1]) << 16);
+    w.y = e[2] | (static_cast<uint32_t>(e[3]) << 16);
+    w.z = e[4] | (static_cast<uint32_t>(e[5]) << 16);
+    w.w = e[6] | (static_cast<uint32_t>(e[7]) << 16);
+    *reinterpret_cast<uint4*>(dst + static_cast<int64_t>(d) * s_pad + s0 + c) = w;
+  }
+  if (__syncthreads_or(range) && threadIdx.x == 0) set_status(dev_status, SA_DEV_RANGE);
+}
+
+template <int D>
+cudaError_t launch_attn_d(const AttnMaps& m, const AttnArgs& a, cudaStream_t st) {
+  constexpr int smem = Smem<D>::kBytes;
+  static_assert(smem <= 227 * 1024, "attention tile does not fit shared memory");
+  cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid(a.n_pairs, a.H, a.B);
+  attn_fwd_kernel<D><<<grid, kThreads, smem, st>>>(m.q, m.k, m.vt, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_pack_v(const uint16_t* v, const int64_t vs[3], int B, int S, int H, int D,
+                          int s_pad, uint16_t* vt, int32_t* dev_status, cudaStream_t st) {
+  dim3 grid((S + kBlock - 1) / kBlock, H, B);
+  if (D == 128)
+    pack_v_kernel<128><<<grid, 256, 0, st>>>(v, vs[0], vs[1], vs[2], S, H, s_pad, vt, dev_status);
+  else
+    pack_v_kernel<64><<<grid, 256, 0, st>>>(v, vs[0], vs[1], vs[2], S, H, s_pad, vt, dev_status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_attn(int D, const AttnMaps& m, const AttnArgs& a, cudaStream_t st) {
+  return D == 128 ? launch_attn_d<128>(m, a, st) : launch_attn_d<64>(m, a, st);
+}
+
+}  // namespace sa

@@ -1,0 +1,479 @@
+// route.cu -- the online block router on sm_103a.
+//
+// The pages name an online router over compressed (block-pooled) queries
+// and keys with threshold tau = 1.0, a diagonal threshold and an exact prefix
+// sink ("MiniMax H3 runs on single 4090 with 4.44x speedup over dense
+// execution", third paragraph; Sol-Engine H3-DataCenter release page, policy
+// paragraph). The rule evaluated here: qbar/kbar = mean of the valid tokens of
+// each 64-token block; s_ij = scale * qbar_i . kbar_j over every key block;
+// p_ij = softmax_j(s_ij); keep j iff p_ij >= tau/Nb, or j is a sink block
+// (j < ceil(P/64)), or j == i.
+//
+// Kernels, in launch order:
+//   pool     Q and K read once; block sums accumulated error-free (TwoSum in
+//            fp32, so the fp64 mean is exact to fp64 rounding); writes fp32
+//            and fp64 pooled vectors and their 2-norms.          HBM-bound.
+//   score    pooled Q . pooled K^T per head, 64x64 fp32 SIMT tiles; writes
+//            the logits and each tile's row max / sum of exponentials.
+//   select   per row: log-sum-exp from the tile partials, threshold test in
+//            log space, forced blocks, a bitmask and a count. A row with a
+//            decision inside the fp32 error bound is queued for recheck.
+//   recheck  queued rows recomputed wholly in fp64 from the fp64 pooled
+//            vectors (the same formula as the definition).
+//   scan     exclusive scan of the counts -> row_ptr.
+//   emit     bitmask -> ascending col_idx, bounded by col_cap.
+#include <cfloat>
+#include <cmath>
+
+#include "ptx.cuh"
+#include "sa_internal.cuh"
+
+namespace sa {
+
+namespace {
+
+__device__ __forceinline__ float bf16_to_f32(uint16_t h) {
+  return __uint_as_float(static_cast<uint32_t>(h) << 16);
+}
+
+// TwoSum: s + e == a + b exactly (round-to-nearest, no overflow).
+__device__ __forceinline__ void two_sum(float& s, float& e, float b) {
+  const float a = s;
+  const float t = __fadd_rn(a, b);
+  const float bb = __fsub_rn(t, a);
+  const float err = __fadd_rn(__fsub_rn(a, __fsub_rn(t, bb)), __fsub_rn(b, bb));
+  s = t;
+  e = __fadd_rn(e, err);
+}
+
+template <typename T>
+__device__ __forceinline__ T* ws_ptr(char* ws, size_t off) {
+  return reinterpret_cast<T*>(ws + off);
+}
+
+// ---------------------------------------------------------------- pool ---
+// grid (Nb, ceil(H*D / 1024), 2*B), 128 threads; each thread owns 8
+// consecutive d of one head (a 16-byte load per token).
+template <int D>
+__global__ void __launch_bounds__(128) pool_kernel(RouteArgs a) {
+  const int i = blockIdx.x;
+  const int which = blockIdx.z & 1;  // 0: Q, 1: K
+  const int b = blockIdx.z >> 1;
+  const int e0 = (blockIdx.y * 128 + threadIdx.x) * 8;
+  const int HD = a.H * D;
+  const bool active = e0 < HD;
+  const int h = active ? e0 / D : 0;
+  const int d = active ? e0 % D : 0;
+  const uint16_t* X = which ? a.k : a.q;
+  const int64_t* st = which ? a.ks : a.qs;
+  const int t0 = i * kBlock;
+  const int n = min(kBlock, a.S - t0);
+
+  float s[8], c[8];
+#pragma unroll
+  for (int u = 0; u < 8; ++u) s[u] = c[u] = 0.f;
+
+  if (active) {
+    const uint16_t* base = X + b * st[0] + h * st[2] + d + t0 * st[1];
+    for (int t = 0; t < n; t += 8) {
+      uint4 buf[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (t + u < n) buf[u] = __ldg(reinterpret_cast<const uint4*>(base + (t + u) * st[1]));
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (t + u < n) {
+          const uint32_t w[4] = {buf[u].x, buf[u].y, buf[u].z, buf[u].w};
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            two_sum(s[2 * v], c[2 * v], bf16_to_f32(static_cast<uint16_t>(w[v] & 0xffffu)));
+            two_sum(s[2 * v + 1], c[2 * v + 1], bf16_to_f32(static_cast<uint16_t>(w[v] >> 16)));
+          }
+        }
+      }
+    }
+  }
+
+  double sq = 0.0;
+  if (active) {
+    const int bh = b * a.H + h;
+    const size_t row = static_cast<size_t>(bh) * a.Nb + i;
+    float* p32 = ws_ptr<float>(a.ws, which ? a.L.kbar32 : a.L.qbar32) + row * D + d;
+    double* p64 = ws_ptr<double>(a.ws, which ? a.L.kbar64 : a.L.qbar64) + row * D + d;
+    double m[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      m[u] = (static_cast<double>(s[u]) + static_cast<double>(c[u])) / static_cast<double>(n);
+      sq += m[u] * m[u];
+    }
+    reinterpret_cast<float4*>(p32)[0] = make_float4(float(m[0]), float(m[1]), float(m[2]), float(m[3]));
+    reinterpret_cast<float4*>(p32)[1] = make_float4(float(m[4]), float(m[5]), float(m[6]), float(m[7]));
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      reinterpret_cast<double2*>(p64)[u] = make_double2(m[2 * u], m[2 * u + 1]);
+  }
+  // 2-norm of the pooled vector: the D/8 threads of one head are adjacent lanes.
+#pragma unroll
+  for (int off = D / 16; off >= 1; off >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, off);
+  if (active && d == 0) {
+    const int bh = b * a.H + h;
+    const size_t row = static_cast<size_t>(bh) * a.Nb + i;
+    const float nrm = static_cast<float>(sqrt(sq) * (1.0 + 1e-6));  // rounded up
+    ws_ptr<float>(a.ws, which ? a.L.knorm : a.L.qnorm)[row] = nrm;
+    if (which) atomicMax(ws_ptr<int>(a.ws, a.L.kmax) + bh, __float_as_int(nrm));
+  }
+}
+
+// --------------------------------------------------------------- score ---
+// grid (n_ct, n_ct, B*H), 256 threads; a 64x64 tile of pooled logits,
+// 4x4 outputs per thread, D consumed in chunks of 32.
+template <int D>
+__global__ void __launch_bounds__(256) score_kernel(RouteArgs a) {
+  constexpr int T = kScoreTile, KC = 32;
+  __shared__ __align__(16) float Qs[KC][T];
+  __shared__ __align__(16) float Ks[KC][T];
+  const int j0 = blockIdx.x * T, i0 = blockIdx.y * T, bh = blockIdx.z;
+  const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
+  const float* qb = ws_ptr<float>(a.ws, a.L.qbar32) + static_cast<size_t>(bh) * a.Nb * D;
+  const float* kb = ws_ptr<float>(a.ws, a.L.kbar32) + static_cast<size_t>(bh) * a.Nb * D;
+
+  float acc[4][4];
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) acc[r][c] = 0.f;
+
+  const int lr = tid >> 2, lc = (tid & 3) * 8;  // loader: row, 8 dims
+  for (int d0 = 0; d0 < D; d0 += KC) {
+    float4 qa = make_float4(0, 0, 0, 0), qb4 = qa, ka = qa, kb4 = qa;
+    if (i0 + lr < a.Nb) {
+      const float4* src = reinterpret_cast<const float4*>(qb + static_cast<size_t>(i0 + lr) * D + d0 + lc);
+      qa = src[0];
+      qb4 = src[1];
+    }
+    if (j0 + lr < a.Nb) {
+      const float4* src = reinterpret_cast<const float4*>(kb + static_cast<size_t>(j0 + lr) * D + d0 + lc);
+      ka = src[0];
+      kb4 = src[1];
+    }
+    __syncthreads();
+    Qs[lc + 0][lr] = qa.x; Qs[lc + 1][lr] = qa.y; Qs[lc + 2][lr] = qa.z; Qs[lc + 3][lr] = qa.w;
+    Qs[lc + 4][lr] = qb4.x; Qs[lc + 5][lr] = qb4.y; Qs[lc + 6][lr] = qb4.z; Qs[lc + 7][lr] = qb4.w;
+    Ks[lc + 0][lr] = ka.x; Ks[lc + 1][lr] = ka.y; Ks[lc + 2][lr] = ka.z; Ks[lc + 3][lr] = ka.w;
+    Ks[lc + 4][lr] = kb4.x; Ks[lc + 5][lr] = kb4.y; Ks[lc + 6][lr] = kb4.z; Ks[lc + 7][lr] = kb4.w;
+    __syncthreads();
+#pragma unroll 8
+    for (int kk = 0; kk < KC; ++kk) {
+      const float4 qv = *reinterpret_cast<const float4*>(&Qs[kk][ty * 4]);
+      const float4 kv = *reinterpret_cast<const float4*>(&Ks[kk][tx * 4]);
+      const float qr[4] = {qv.x, qv.y, qv.z, qv.w};
+      const float kc[4] = {kv.x, kv.y, kv.z, kv.w};
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[r][c] = fmaf(qr[r], kc[c], acc[r][c]);
+    }
+  }
+
+  float* scores = ws_ptr<float>(a.ws, a.L.scores);
+  float* pm = ws_ptr<float>(a.ws, a.L.part_m);
+  float* ps = ws_ptr<float>(a.ws, a.L.part_s);
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const int i = i0 + ty * 4 + r;
+    float sv[4];
+    float mx = -INFINITY;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int j = j0 + tx * 4 + c;
+      sv[c] = acc[r][c] * a.scale;
+      if (j < a.Nb) mx = fmaxf(mx, sv[c]);
+    }
+#pragma unroll
+    for (int off = 8; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    float se = 0.f;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int j = j0 + tx * 4 + c;
+      if (j < a.Nb) se += expf(sv[c] - mx);
+    }
+#pragma unroll
+    for (int off = 8; off >= 1; off >>= 1) se += __shfl_xor_sync(0xffffffffu, se, off);
+    if (i < a.Nb) {
+      const size_t row = static_cast<size_t>(bh) * a.Nb + i;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int j = j0 + tx * 4 + c;
+        if (j < a.Nb) scores[row * a.Nb + j] = sv[c];
+      }
+      if (tx == 0) {
+        pm[row * a.n_ct + blockIdx.x] = mx;
+        ps[row * a.n_ct + blockIdx.x] = se;
+      }
+    }
+  }
+}
+
+// -------------------------------------------------------------- select ---
+// one warp per row (b, h, i); 8 rows per 256-thread CTA.
+__global__ void __launch_bounds__(256) select_kernel(RouteArgs a) {
+  const unsigned full = 0xffffffffu;
+  const int lane = threadIdx.x & 31;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  if (row >= a.L.rows) return;
+  const int bh = static_cast<int>(row / a.Nb);
+  const int i = static_cast<int>(row % a.Nb);
+  uint32_t* bits = ws_ptr<uint32_t>(a.ws, a.L.bits) + row * a.words;
+  int cnt = 0;
+  bool flag = false;
+
+  if (a.keep_all) {
+    for (int w = 0; w < a.words; ++w) {
+      const int j = w * 32 + lane;
+      const uint32_t m = __ballot_sync(full, j < a.Nb);
+      if (lane == 0) bits[w] = m;
+      cnt += __popc(m);
+    }
+  } else {
+    const float* pm = ws_ptr<float>(a.ws, a.L.part_m) + row * a.n_ct;
+    const float* ps = ws_ptr<float>(a.ws, a.L.part_s) + row * a.n_ct;
+    float M = -INFINITY;
+    for (int c = lane; c < a.n_ct; c += 32) M = fmaxf(M, pm[c]);
+    for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(full, M, off));
+    float Z = 0.f;
+    for (int c = lane; c < a.n_ct; c += 32) Z += ps[c] * expf(pm[c] - M);
+    for (int off = 16; off >= 1; off >>= 1) Z += __shfl_xor_sync(full, Z, off);
+    const float T = M + logf(Z) + a.log_tau_over_nb;
+    const float qn = ws_ptr<float>(a.ws, a.L.qnorm)[row];
+    const float kmx = __int_as_float(ws_ptr<int>(a.ws, a.L.kmax)[bh]);
+    const float* kn = ws_ptr<float>(a.ws, a.L.knorm) + static_cast<size_t>(bh) * a.Nb;
+    const float gq = a.gamma * a.scale * qn;
+    const float err_row = gq * kmx + 1e-5f * (1.f + fabsf(T));
+    const float* srow = ws_ptr<float>(a.ws, a.L.scores) + row * a.Nb;
+    for (int w = 0; w < a.words; ++w) {
+      const int j = w * 32 + lane;
+      bool keep = false;
+      if (j < a.Nb) {
+        const bool forced = (j < a.n_sink) || (j == i);
+        const float margin = srow[j] - T;
+        keep = forced || (margin >= 0.f);
+        if (!forced && fabsf(margin) <= fmaf(gq, kn[j], err_row)) flag = true;
+      }
+      const uint32_t m = __ballot_sync(full, keep);
+      if (lane == 0) bits[w] = m;
+      cnt += __popc(m);
+    }
+  }
+  flag = __any_sync(full, flag);
+  if (lane == 0) {
+    ws_ptr<int>(a.ws, a.L.counts)[row] = cnt;
+    if (flag) {
+      const int slot = atomicAdd(ws_ptr<int>(a.ws, a.L.nflag), 1);
+      ws_ptr<int>(a.ws, a.L.flags)[slot] = static_cast<int>(row);
+    }
+  }
+}
+
+// ------------------------------------------------------------- recheck ---
+// grid-stride over the queued rows; 128 threads; fp64 throughout.
+template <int D>
+__global__ void __launch_bounds__(128) recheck_kernel(RouteArgs a) {
+  extern __shared__ __align__(16) double rs[];  // [D] qbar64 row, then [Nb] logits
+  __shared__ double red[4];
+  __shared__ int redc[4];
+  const unsigned full = 0xffffffffu;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  double* qrow = rs;
+  double* s64 = rs + D;
+  const int nflag = *ws_ptr<int>(a.ws, a.L.nflag);
+  const double* kb64 = ws_ptr<double>(a.ws, a.L.kbar64);
+  const double* qb64 = ws_ptr<double>(a.ws, a.L.qbar64);
+
+  for (int f = blockIdx.x; f < nflag; f += gridDim.x) {
+    const int64_t row = ws_ptr<int>(a.ws, a.L.flags)[f];
+    const int bh = static_cast<int>(row / a.Nb);
+    const int i = static_cast<int>(row % a.Nb);
+    for (int d = threadIdx.x; d < D; d += 128) qrow[d] = qb64[row * D + d];
+    __syncthreads();
+    for (int k = warp; k < a.Nb; k += 4) {
+      const double* kr = kb64 + (static_cast<size_t>(bh) * a.Nb + k) * D;
+      double acc = 0.0;
+#pragma unroll
+      for (int d = lane; d < D; d += 32) acc = fma(qrow[d], kr[d], acc);
+      for (int off = 16; off >= 1; off >>= 1) acc += __shfl_xor_sync(full, acc, off);
+      if (lane == 0) s64[k] = a.scale64 * acc;
+    }
+    __syncthreads();
+    double m = -INFINITY;
+    for (int k = threadIdx.x; k < a.Nb; k += 128) m = fmax(m, s64[k]);
+    for (int off = 16; off >= 1; off >>= 1) m = fmax(m, __shfl_xor_sync(full, m, off));
+    if (lane == 0) red[warp] = m;
+    __syncthreads();
+    m = fmax(fmax(red[0], red[1]), fmax(red[2], red[3]));
+    __syncthreads();
+    double z = 0.0;
+    for (int k = threadIdx.x; k < a.Nb; k += 128) z += exp(s64[k] - m);
+    for (int off = 16; off >= 1; off >>= 1) z += __shfl_xor_sync(full, z, off);
+    if (lane == 0) red[warp] = z;
+    __syncthreads();
+    z = (red[0] + red[1]) + (red[2] + red[3]);
+    uint32_t* bits = ws_ptr<uint32_t>(a.ws, a.L.bits) + row * a.words;
+    int cnt = 0;
+    for (int w = warp; w < a.words; w += 4) {
+      const int j = w * 32 + lane;
+      bool keep = false;
+      if (j < a.Nb) {
+        const bool forced = (j < a.n_sink) || (j == i);
+        keep = forced || (exp(s64[j] - m) / z >= a.tau_over_nb);
+      }
+      const uint32_t bm = __ballot_sync(full, keep);
+      if (lane == 0) bits[w] = bm;
+      cnt += __popc(bm);
+    }
+    if (lane == 0) redc[warp] = cnt;
+    __syncthreads();
+    if (threadIdx.x == 0)
+      ws_ptr<int>(a.ws, a.L.counts)[row] = redc[0] + redc[1] + redc[2] + redc[3];
+    __syncthreads();
+  }
+}
+
+// ---------------------------------------------------------------- scan ---
+// one CTA of 1024 threads: row_ptr = exclusive scan of counts.
+__global__ void __launch_bounds__(1024) scan_kernel(RouteArgs a) {
+  __shared__ int64_t wsum[32];
+  const int64_t n = a.L.rows;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t per = (n + 1023) / 1024;
+  const int64_t lo = min(n, tid * per), hi = min(n, lo + per);
+  const int* counts = ws_ptr<int>(a.ws, a.L.counts);
+  int64_t local = 0;
+  for (int64_t r = lo; r < hi; ++r) local += counts[r];
+  int64_t incl = local;
+  for (int off = 1; off < 32; off <<= 1) {
+    const int64_t v = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += v;
+  }
+  if (lane == 31) wsum[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int64_t v = wsum[lane];
+    for (int off = 1; off < 32; off <<= 1) {
+      const int64_t u = __shfl_up_sync(0xffffffffu, v, off);
+      if (lane >= off) v += u;
+    }
+    wsum[lane] = v;  // inclusive over warps
+  }
+  __syncthreads();
+  int64_t run = incl - local + (warp > 0 ? wsum[warp - 1] : 0);
+  for (int64_t r = lo; r < hi; ++r) {
+    a.row_ptr[r] = static_cast<int32_t>(run);
+    run += counts[r];
+  }
+  if (tid == 1023) a.row_ptr[n] = static_cast<int32_t>(wsum[31]);
+}
+
+// ---------------------------------------------------------------- emit ---
+// one warp per row: set bits of the row's mask -> ascending key blocks.
+__global__ void __launch_bounds__(256) emit_kernel(RouteArgs a) {
+  const unsigned full = 0xffffffffu;
+  const int lane = threadIdx.x & 31;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  if (row >= a.L.rows) return;
+  const uint32_t* bits = ws_ptr<uint32_t>(a.ws, a.L.bits) + row * a.words;
+  int64_t base = a.row_ptr[row];
+  bool overflow = false;
+  for (int w0 = 0; w0 < a.words; w0 += 32) {
+    const int w = w0 + lane;
+    uint32_t u = (w < a.words) ? bits[w] : 0u;
+    const int c = __popc(u);
+    int incl = c;
+    for (int off = 1; off < 32; off <<= 1) {
+      const int v = __shfl_up_sync(full, incl, off);
+      if (lane >= off) incl += v;
+    }
+    int64_t pos = base + (incl - c);
+    while (u) {
+      const int bpos = __ffs(u) - 1;
+      if (pos < a.col_cap) a.col_idx[pos] = w * 32 + bpos;
+      else overflow = true;
+      ++pos;
+      u &= u - 1;
+    }
+    base += __shfl_sync(full, incl, 31);
+  }
+  if (__any_sync(full, overflow) && lane == 0 && a.dev_status)
+    atomicOr(a.dev_status, SA_DEV_CAPACITY);
+}
+
+template <int D>
+cudaError_t launch_route_d(const RouteArgs& a, cudaStream_t st) {
+  const RouteLayout& L = a.L;
+  cudaError_t e = cudaMemsetAsync(a.ws + L.nflag, 0, sizeof(int), st);
+  if (e != cudaSuccess) return e;
+  e = cudaMemsetAsync(a.ws + L.kmax, 0, sizeof(int) * static_cast<size_t>(a.B) * a.H, st);
+  if (e != cudaSuccess) return e;
+  {
+    dim3 grid(a.Nb, (a.H * D + 1023) / 1024, 2 * a.B);
+    pool_kernel<D><<<grid, 128, 0, st>>>(a);
+  }
+  {
+    dim3 grid(a.n_ct, a.n_ct, a.B * a.H);
+    score_kernel<D><<<grid, 256, 0, st>>>(a);
+  }
+  const unsigned row_ctas = static_cast<unsigned>((L.rows + 7) / 8);
+  select_kernel<<<row_ctas, 256, 0, st>>>(a);
+  {
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const size_t smem = sizeof(double) * (D + a.Nb);
+    if (smem > 48 * 1024) {
+      e = cudaFuncSetAttribute(recheck_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(smem));
+      if (e != cudaSuccess) return e;
+    }
+    recheck_kernel<D><<<2 * sms, 128, smem, st>>>(a);
+  }
+  scan_kernel<<<1, 1024, 0, st>>>(a);
+  emit_kernel<<<row_ctas, 256, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+static size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+RouteLayout route_layout(const sa_params& p) {
+  RouteLayout L{};
+  L.Nb = num_blocks(p.S);
+  L.n_ct = (L.Nb + kScoreTile - 1) / kScoreTile;
+  L.words = (L.Nb + 31) / 32;
+  const size_t bh = static_cast<size_t>(p.B) * p.H;
+  L.rows = static_cast<int64_t>(bh) * L.Nb;
+  const size_t rows = static_cast<size_t>(L.rows);
+  size_t off = 0;
+  auto take = [&](size_t bytes) { const size_t o = off; off = align256(off + bytes); return o; };
+  L.qbar32 = take(rows * p.D * sizeof(float));
+  L.kbar32 = take(rows * p.D * sizeof(float));
+  L.qbar64 = take(rows * p.D * sizeof(double));
+  L.kbar64 = take(rows * p.D * sizeof(double));
+  L.qnorm = take(rows * sizeof(float));
+  L.knorm = take(rows * sizeof(float));
+  L.kmax = take(bh * sizeof(int));
+  L.part_m = take(rows * L.n_ct * sizeof(float));
+  L.part_s = take(rows * L.n_ct * sizeof(float));
+  L.scores = take(rows * static_cast<size_t>(L.Nb) * sizeof(float));
+  L.bits = take(rows * L.words * sizeof(uint32_t));
+  L.counts = take(rows * sizeof(int));
+  L.nflag = take(sizeof(int));
+  L.flags = take(rows * sizeof(int));
+  L.total = off;
+  return L;
+}
+
+cudaError_t launch_route(const RouteArgs& a, cudaStream_t st) {
+  return a.D == 128 ? launch_route_d<128>(a, st) : launch_route_d<64>(a, st);
+}
+
+}  // namespace sa

@@ -1,0 +1,314 @@
+// sa_api.cu -- the extern "C" boundary: argument checks, workspace layout,
+// TMA descriptor encoding and the launch sequence of each entry point.
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "sa_internal.cuh"
+
+namespace sa {
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool strides_ok(const int64_t s[3]) {
+  for (int i = 0; i < 3; ++i)
+    if (s[i] <= 0 || (s[i] & 7) != 0) return false;
+  return true;
+}
+
+sa_status check_params(const sa_params* p) {
+  if (!p) return SA_ERR_INVALID_ARG;
+  if (p->B < 1 || p->S < 1 || p->H < 1 || p->block != kBlock) return SA_ERR_INVALID_ARG;
+  if (p->prefix_len < 0 || p->prefix_len > p->S) return SA_ERR_INVALID_ARG;
+  if (!(p->tau >= 0.f) || !std::isfinite(p->tau)) return SA_ERR_INVALID_ARG;
+  if (!(p->softmax_scale >= 0.f) || !std::isfinite(p->softmax_scale)) return SA_ERR_INVALID_ARG;
+  if (p->D != 64 && p->D != 128) return p->D > 0 ? SA_ERR_UNSUPPORTED : SA_ERR_INVALID_ARG;
+  if (p->H > 65535 || p->B > 65535) return SA_ERR_UNSUPPORTED;
+  const int64_t nb = num_blocks(p->S);
+  const int64_t max_nnz = static_cast<int64_t>(p->B) * p->H * nb * nb;
+  if (max_nnz > INT32_MAX) return SA_ERR_UNSUPPORTED;  // row_ptr is int32
+  return SA_OK;
+}
+
+double scale64_of(const sa_params* p) {
+  return p->softmax_scale > 0.f ? static_cast<double>(p->softmax_scale)
+                                : 1.0 / std::sqrt(static_cast<double>(p->D));
+}
+
+sa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? SA_OK : SA_ERR_CUDA; }
+
+int s_pad_of(int S) { return (S + 7) & ~7; }
+
+// [B, S, H, D] bf16 -> 4-D map (D, S, H, B), box 64 x 64, 128-byte swizzle.
+sa_status encode_bshd(CUtensorMap* m, const void* base, const sa_params* p, const int64_t st[3]) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return SA_ERR_CUDA;
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(p->D), static_cast<cuuint64_t>(p->S),
+                              static_cast<cuuint64_t>(p->H), static_cast<cuuint64_t>(p->B)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(st[1]) * 2,
+                                 static_cast<cuuint64_t>(st[2]) * 2,
+                                 static_cast<cuuint64_t>(st[0]) * 2};
+  const cuuint32_t box[4] = {64, 64, 1, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? SA_OK : SA_ERR_INVALID_ARG;
+}
+
+// vt [B*H][D][s_pad] fp16 -> 3-D map (S, D, B*H), box 64 keys x D rows.
+sa_status encode_vt(CUtensorMap* m, const void* base, const sa_params* p) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return SA_ERR_CUDA;
+  const cuuint64_t sp = static_cast<cuuint64_t>(s_pad_of(p->S));
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(p->S), static_cast<cuuint64_t>(p->D),
+                              static_cast<cuuint64_t>(p->B) * p->H};
+  const cuuint64_t strides[2] = {sp * 2, sp * 2 * static_cast<cuuint64_t>(p->D)};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(p->D), 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? SA_OK : SA_ERR_INVALID_ARG;
+}
+
+size_t attn_ws_bytes(const sa_params* p) {
+  return static_cast<size_t>(p->B) * p->H * p->D * s_pad_of(p->S) * 2;
+}
+
+sa_status attn_common(const sa_params* p, const void* q, const void* k, const void* v,
+                      const int32_t* row_ptr, const int32_t* col_idx, void* o, float* lse,
+                      void* ws, size_t ws_bytes, int32_t* dev_status, void* stream, bool dense) {
+  sa_status s = check_params(p);
+  if (s != SA_OK) return s;
+  if (!q || !k || !v || !o || !ws) return SA_ERR_INVALID_ARG;
+  if (!dense && (!row_ptr || !col_idx)) return SA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return SA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return SA_ERR_INVALID_ARG;
+  if (!strides_ok(p->q_stride) || !strides_ok(p->k_stride) || !strides_ok(p->v_stride) ||
+      !strides_ok(p->o_stride))
+    return SA_ERR_INVALID_ARG;
+  const int Nb = num_blocks(p->S);
+  if (Nb > kMaxNbAttn) return SA_ERR_UNSUPPORTED;
+  if (ws_bytes < attn_ws_bytes(p)) return SA_ERR_CAPACITY;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+  AttnMaps maps;
+  std::memset(&maps, 0, sizeof(maps));
+  if ((s = encode_bshd(&maps.q, q, p, p->q_stride)) != SA_OK) return s;
+  if ((s = encode_bshd(&maps.k, k, p, p->k_stride)) != SA_OK) return s;
+  if ((s = encode_vt(&maps.vt, ws, p)) != SA_OK) return s;
+
+  cudaError_t e = launch_pack_v(static_cast<const uint16_t*>(v), p->v_stride, p->B, p->S, p->H,
+                                p->D, s_pad_of(p->S), static_cast<uint16_t*>(ws), dev_status, st);
+  if (e != cudaSuccess) return SA_ERR_CUDA;
+
+  AttnArgs a{};
+  a.row_ptr = dense ? nullptr : row_ptr;
+  a.col_idx = dense ? nullptr : col_idx;
+  a.o = static_cast<uint16_t*>(o);
+  a.lse = lse;
+  a.dev_status = dev_status;
+  for (int i = 0; i < 3; ++i) a.os[i] = p->o_stride[i];
+  a.B = p->B;
+  a.S = p->S;
+  a.H = p->H;
+  a.Nb = Nb;
+  a.n_pairs = (Nb + 1) / 2;
+  a.scale_log2 = static_cast<float>(scale64_of(p) * 1.4426950408889634);
+  return from_cuda(launch_attn(p->D, maps, a, st));
+}
+
+}  // namespace
+}  // namespace sa
+
+using namespace sa;
+
+extern "C" {
+
+void sa_params_init(sa_params* p, int32_t B, int32_t S, int32_t H, int32_t D, int32_t prefix_len,
+                    float tau) {
+  if (!p) return;
+  std::memset(p, 0, sizeof(*p));
+  p->B = B;
+  p->S = S;
+  p->H = H;
+  p->D = D;
+  p->block = kBlock;
+  p->prefix_len = prefix_len;
+  p->tau = tau;
+  p->softmax_scale = 0.f;
+  const int64_t st[3] = {static_cast<int64_t>(S) * H * D, static_cast<int64_t>(H) * D, D};
+  for (int i = 0; i < 3; ++i) {
+    p->q_stride[i] = st[i];
+    p->k_stride[i] = st[i];
+    p->v_stride[i] = st[i];
+    p->o_stride[i] = st[i];
+  }
+}
+
+int32_t sa_num_blocks(const sa_params* p) {
+  return (p && p->S >= 1) ? num_blocks(p->S) : 0;
+}
+
+int64_t sa_route_rows(const sa_params* p) {
+  if (check_params(p) != SA_OK) return 0;
+  return static_cast<int64_t>(p->B) * p->H * num_blocks(p->S);
+}
+
+int64_t sa_route_max_nnz(const sa_params* p) {
+  if (check_params(p) != SA_OK) return 0;
+  const int64_t nb = num_blocks(p->S);
+  return static_cast<int64_t>(p->B) * p->H * nb * nb;
+}
+
+size_t sa_route_workspace_bytes(const sa_params* p) {
+  if (check_params(p) != SA_OK) return 0;
+  return route_layout(*p).total;
+}
+
+size_t sa_attn_workspace_bytes(const sa_params* p) {
+  if (check_params(p) != SA_OK) return 0;
+  return attn_ws_bytes(p);
+}
+
+sa_status sa_route(const sa_params* p, const void* q, const void* k, int32_t* row_ptr,
+                   int32_t* col_idx, int64_t col_cap, void* workspace, size_t ws_bytes,
+                   int32_t* dev_status, void* stream) {
+  sa_status s = check_params(p);
+  if (s != SA_OK) return s;
+  if (!q || !k || !row_ptr || !col_idx || !workspace || col_cap < 0) return SA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k)) return SA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return SA_ERR_INVALID_ARG;
+  if (!strides_ok(p->q_stride) || !strides_ok(p->k_stride)) return SA_ERR_INVALID_ARG;
+  const RouteLayout L = route_layout(*p);
+  if (ws_bytes < L.total) return SA_ERR_CAPACITY;
+
+  RouteArgs a{};
+  a.q = static_cast<const uint16_t*>(q);
+  a.k = static_cast<const uint16_t*>(k);
+  for (int i = 0; i < 3; ++i) {
+    a.qs[i] = p->q_stride[i];
+    a.ks[i] = p->k_stride[i];
+  }
+  a.B = p->B;
+  a.S = p->S;
+  a.H = p->H;
+  a.D = p->D;
+  a.Nb = L.Nb;
+  a.n_ct = L.n_ct;
+  a.words = L.words;
+  a.n_sink = (p->prefix_len + kBlock - 1) / kBlock;
+  a.scale64 = scale64_of(p);
+  a.scale = static_cast<float>(a.scale64);
+  a.keep_all = p->tau == 0.f;
+  a.tau_over_nb = static_cast<double>(p->tau) / L.Nb;
+  a.log_tau_over_nb = a.keep_all ? 0.f
+                                 : static_cast<float>(std::log(static_cast<double>(p->tau)) -
+                                                      std::log(static_cast<double>(L.Nb)));
+  // gamma_{D+3} (1 + 1%) with u = 2^-24: bounds the fp32 pooled dot product
+  // error by gamma * scale * |qbar| |kbar|.
+  const double u = std::ldexp(1.0, -24), n = p->D + 3;
+  a.gamma = static_cast<float>(1.01 * n * u / (1.0 - n * u));
+  a.ws = static_cast<char*>(workspace);
+  a.L = L;
+  a.row_ptr = row_ptr;
+  a.col_idx = col_idx;
+  a.col_cap = col_cap;
+  a.dev_status = dev_status;
+  return from_cuda(launch_route(a, static_cast<cudaStream_t>(stream)));
+}
+
+sa_status sa_attn_sparse(const sa_params* p, const void* q, const void* k, const void* v,
+                         const int32_t* row_ptr, const int32_t* col_idx, void* o, float* lse,
+                         void* workspace, size_t ws_bytes, int32_t* dev_status, void* stream) {
+  return attn_common(p, q, k, v, row_ptr, col_idx, o, lse, workspace, ws_bytes, dev_status, stream,
+                     false);
+}
+
+sa_status sa_attn_dense(const sa_params* p, const void* q, const void* k, const void* v, void* o,
+                        float* lse, void* workspace, size_t ws_bytes, int32_t* dev_status,
+                        void* stream) {
+  return attn_common(p, q, k, v, nullptr, nullptr, o, lse, workspace, ws_bytes, dev_status, stream,
+                     true);
+}
+
+sa_status sa_forward_host(const sa_params* p, const void* q_host, const void* k_host,
+                          const void* v_host, void* o_host, float* lse_host, void* q_dev,
+                          void* k_dev, void* v_dev, void* o_dev, float* lse_dev, int32_t* row_ptr,
+                          int32_t* col_idx, int64_t col_cap, void* workspace, size_t ws_bytes,
+                          int32_t* dev_status, void* stream) {
+  sa_status s = check_params(p);
+  if (s != SA_OK) return s;
+  if (!q_host || !k_host || !v_host || !o_host || !q_dev || !k_dev || !v_dev || !o_dev)
+    return SA_ERR_INVALID_ARG;
+  const int64_t cont[3] = {static_cast<int64_t>(p->S) * p->H * p->D,
+                           static_cast<int64_t>(p->H) * p->D, p->D};
+  for (int i = 0; i < 3; ++i)
+    if (p->q_stride[i] != cont[i] || p->k_stride[i] != cont[i] || p->v_stride[i] != cont[i] ||
+        p->o_stride[i] != cont[i])
+      return SA_ERR_INVALID_ARG;
+  const size_t bytes = static_cast<size_t>(p->B) * cont[0] * 2;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(q_dev, q_host, bytes, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+      cudaMemcpyAsync(k_dev, k_host, bytes, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+      cudaMemcpyAsync(v_dev, v_host, bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
+    return SA_ERR_CUDA;
+  s = sa_route(p, q_dev, k_dev, row_ptr, col_idx, col_cap, workspace, ws_bytes, dev_status, stream);
+  if (s != SA_OK) return s;
+  s = sa_attn_sparse(p, q_dev, k_dev, v_dev, row_ptr, col_idx, o_dev, lse_dev, workspace, ws_bytes,
+                     dev_status, stream);
+  if (s != SA_OK) return s;
+  if (cudaMemcpyAsync(o_host, o_dev, bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return SA_ERR_CUDA;
+  if (lse_host && lse_dev) {
+    const size_t lb = static_cast<size_t>(p->B) * p->H * p->S * sizeof(float);
+    if (cudaMemcpyAsync(lse_host, lse_dev, lb, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+      return SA_ERR_CUDA;
+  }
+  return SA_OK;
+}
+
+sa_status sa_dev_status_decode(int32_t d) {
+  if (d & SA_DEV_TIMEOUT) return SA_ERR_TIMEOUT;
+  if (d & SA_DEV_BAD_ROUTE) return SA_ERR_INVALID_ARG;
+  if (d & SA_DEV_CAPACITY) return SA_ERR_CAPACITY;
+  if (d & SA_DEV_RANGE) return SA_ERR_UNSUPPORTED;
+  return SA_OK;
+}
+
+const char* sa_status_string(sa_status s) {
+  switch (s) {
+    case SA_OK: return "SA_OK";
+    case SA_ERR_INVALID_ARG: return "SA_ERR_INVALID_ARG";
+    case SA_ERR_UNSUPPORTED: return "SA_ERR_UNSUPPORTED";
+    case SA_ERR_CAPACITY: return "SA_ERR_CAPACITY";
+    case SA_ERR_CUDA: return "SA_ERR_CUDA";
+    case SA_ERR_TIMEOUT: return "SA_ERR_TIMEOUT";
+  }
+  return "SA_ERR_UNKNOWN";
+}
+
+}  // extern "C"

@@ -1,0 +1,74 @@
+// sa_internal.cuh -- shared between the C-ABI host code and the kernels.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/sa.h"
+
+namespace sa {
+
+constexpr int kBlock = 64;          // query/key block (tokens)
+constexpr int kMaxNbAttn = 4096;    // key blocks the attention tile can list
+constexpr int kScoreTile = 64;      // pooled-score tile (query blocks x key blocks)
+
+inline int num_blocks(int S) { return (S + kBlock - 1) / kBlock; }
+
+// ------------------------------------------------------------ routing ---
+
+struct RouteLayout {      // byte offsets into the caller's route workspace
+  size_t qbar32, kbar32, qbar64, kbar64, qnorm, knorm, kmax;
+  size_t part_m, part_s, scores, bits, counts, nflag, flags, total;
+  int Nb, n_ct, words;
+  int64_t rows;
+};
+
+RouteLayout route_layout(const sa_params& p);
+
+struct RouteArgs {
+  const uint16_t* q;      // bf16 bits
+  const uint16_t* k;
+  int64_t qs[3], ks[3];   // element strides of b, s, h
+  int B, S, H, D, Nb, n_ct, words, n_sink;
+  float scale;            // fp32 softmax scale
+  double scale64;         // fp64 softmax scale
+  float log_tau_over_nb;  // logf(tau) - logf(Nb)  (tau > 0)
+  double tau_over_nb;     // tau / Nb in fp64
+  int keep_all;           // tau == 0
+  float gamma;            // fp32 dot-product error constant
+  char* ws;
+  RouteLayout L;
+  int32_t* row_ptr;
+  int32_t* col_idx;
+  int64_t col_cap;
+  int32_t* dev_status;
+};
+
+cudaError_t launch_route(const RouteArgs& a, cudaStream_t st);
+
+// ---------------------------------------------------------- attention ---
+
+struct AttnArgs {
+  const int32_t* row_ptr;  // nullptr: dense (every key block)
+  const int32_t* col_idx;
+  uint16_t* o;             // bf16 bits
+  float* lse;
+  int32_t* dev_status;
+  int64_t os[3];
+  int B, S, H, Nb, n_pairs;
+  float scale_log2;        // softmax_scale * log2(e)
+};
+
+struct AttnMaps {
+  CUtensorMap q, k, vt;
+};
+
+// Repacks V [B,S,H,D] bf16 into vt [B*H][D][s_pad] fp16 (key-contiguous).
+cudaError_t launch_pack_v(const uint16_t* v, const int64_t vs[3], int B, int S, int H, int D,
+                          int s_pad, uint16_t* vt, int32_t* dev_status, cudaStream_t st);
+
+cudaError_t launch_attn(int D, const AttnMaps& maps, const AttnArgs& a, cudaStream_t st);
+
+}  // namespace sa

@@ -1,0 +1,199 @@
+/*
+ * sa.h -- C ABI of the GB300 (sm_103a) routed block-sparse self-attention
+ * library (libsa_gb300.so).
+ *
+ * The layer: one packed sequence per batch entry, [B, S, H, D] bf16 Q/K/V
+ * ("MiniMax H3 runs on single 4090 with 4.44x speedup over dense execution",
+ * third paragraph: [1, 38247, 56, 128], tau = 1.0, diagonal, exact prefix
+ * KV sink, compressed prefix queries; Sol-Engine H3-DataCenter release page,
+ * policy paragraph: a 951-token exact prefix sink, no token reordering, the
+ * first steps and layers dense).
+ *
+ * Conventions shared by every entry point:
+ *  - Device pointers are device memory of the current CUDA device; host
+ *    pointers are named *_host. The caller owns every buffer. Apart from
+ *    sa_forward_host's copies, the library never allocates, frees or
+ *    synchronises: every call enqueues work on `stream` (a cudaStream_t
+ *    passed as void*; NULL = the legacy default stream) and returns.
+ *  - The returned sa_status reports what can be checked before launch
+ *    (arguments, support, launch errors). Conditions found on the device are
+ *    OR-ed into *dev_status (an int32 in device memory that the caller sets
+ *    to 0 before the first call and reads after the stream; NULL = do not
+ *    report) as SA_DEV_* bits. The kernels never trap.
+ *  - Tensors are [B, S, H, D] with the d index contiguous; the strides for
+ *    b, s and h are given in elements and must be multiples of 8 (16 bytes),
+ *    and every tensor base must be 16-byte aligned.
+ *  - Query and key blocks are contiguous 64-token ranges; Nb = ceil(S/64);
+ *    the last block holds S - 64 (Nb - 1) valid tokens. Tokens at or beyond S
+ *    never contribute (the padding contributes exactly zero: "Making
+ *    MiniMax-H3 up to 9x faster on H100s", section "The benchmark was not the
+ *    product").
+ */
+#ifndef SA_GB300_H
+#define SA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum sa_status {
+  SA_OK = 0,
+  SA_ERR_INVALID_ARG = 1, /* a NULL pointer, a bad size, stride or alignment   */
+  SA_ERR_UNSUPPORTED = 2, /* a valid request this build does not serve (D)     */
+  SA_ERR_CAPACITY = 3,    /* a buffer or workspace is smaller than required    */
+  SA_ERR_CUDA = 4,        /* a CUDA runtime or driver call failed              */
+  SA_ERR_TIMEOUT = 5      /* (decoded from dev_status) a bounded wait expired  */
+} sa_status;
+
+/* Bits OR-ed into *dev_status by the kernels. */
+enum {
+  SA_DEV_CAPACITY = 1 << 0, /* the route had more than col_cap entries; the
+                               CSR is truncated (row_ptr is still exact)      */
+  SA_DEV_TIMEOUT = 1 << 1,  /* a bounded pipeline wait gave up; the output of
+                               the affected tiles is undefined                */
+  SA_DEV_BAD_ROUTE = 1 << 2,/* sa_attn_sparse met a row that is not ascending,
+                               has an index outside [0, Nb) or a bad row_ptr;
+                               that row is skipped                            */
+  SA_DEV_RANGE = 1 << 3     /* a V value does not fit fp16 (|v| > 65504); the
+                               P.V product runs in fp16, see sa_attn_sparse    */
+};
+
+typedef struct sa_params {
+  int32_t B, S, H, D;     /* D must be 64 or 128; B, S, H >= 1               */
+  int32_t block;          /* must be 64                                       */
+  int32_t prefix_len;     /* P, 0 <= P <= S: key tokens [0, P) are always
+                             attended, via every key block j < ceil(P/64)    */
+  float tau;              /* router threshold, >= 0; 0 keeps every block     */
+  float softmax_scale;    /* 0 => 1/sqrt(D); used for routing and attention  */
+  int64_t q_stride[3];    /* element strides of b, s, h (d is contiguous)    */
+  int64_t k_stride[3];
+  int64_t v_stride[3];
+  int64_t o_stride[3];
+} sa_params;
+
+/* Fills p for a contiguous [B, S, H, D] layout of all four tensors. */
+void sa_params_init(sa_params* p, int32_t B, int32_t S, int32_t H, int32_t D,
+                    int32_t prefix_len, float tau);
+
+/* Nb = ceil(S / 64) (0 on bad params). */
+int32_t sa_num_blocks(const sa_params* p);
+
+/* Number of CSR rows, B*H*Nb; row_ptr holds this + 1 entries. */
+int64_t sa_route_rows(const sa_params* p);
+
+/* Worst-case number of route entries, B*H*Nb*Nb (every block kept). */
+int64_t sa_route_max_nnz(const sa_params* p);
+
+/* Bytes of device workspace sa_route needs (256-byte aligned start). */
+size_t sa_route_workspace_bytes(const sa_params* p);
+
+/*
+ * sa_route -- the online router: for every (b, h, query block i) the
+ * ascending list of key blocks that query block i attends.
+ *
+ * Rule (the pages name an online router with threshold tau over compressed
+ * queries and keys, a diagonal threshold and an exact prefix sink; the exact
+ * formula is this library's reading of them):
+ *   qbar_i, kbar_j = mean of the valid Q / K tokens of block i / j;
+ *   s_ij = softmax_scale * qbar_i . kbar_j for every key block j;
+ *   p_ij = softmax over j of s_ij;
+ *   keep j  iff  p_ij >= tau / Nb,  or j < ceil(P/64) (sink),  or j == i.
+ * Decisions match an fp64 evaluation of the rule except where
+ * |p_ij * Nb / tau - 1| <= 1e-6 (ties). Pooling is exact to fp64 rounding;
+ * the scores are computed in fp32 and every row holding a decision whose
+ * fp32 margin is inside a rigorous error bound is recomputed in fp64.
+ *
+ * q, k       device, bf16 [B, S, H, D] with the strides in p; not modified.
+ * row_ptr    device int32 [B*H*Nb + 1]; row r = (b*H + h)*Nb + i.
+ *            row_ptr[0] = 0, row_ptr[r+1] - row_ptr[r] = entries of row r.
+ * col_idx    device int32 [col_cap]; the key blocks of row r, ascending, at
+ *            col_idx[row_ptr[r] .. row_ptr[r+1]).
+ * col_cap    capacity of col_idx. If the route is longer, entries beyond
+ *            col_cap are dropped and SA_DEV_CAPACITY is raised; passing
+ *            sa_route_max_nnz(p) can never overflow.
+ * workspace  device scratch of at least sa_route_workspace_bytes(p) bytes,
+ *            256-byte aligned; its contents on entry do not matter.
+ * Errors: SA_ERR_INVALID_ARG / SA_ERR_UNSUPPORTED / SA_ERR_CAPACITY (ws
+ * too small) before launch; SA_ERR_CUDA if a launch fails.
+ */
+sa_status sa_route(const sa_params* p, const void* q, const void* k,
+                   int32_t* row_ptr, int32_t* col_idx, int64_t col_cap,
+                   void* workspace, size_t ws_bytes, int32_t* dev_status,
+                   void* stream);
+
+/* Bytes of device workspace sa_attn_sparse / sa_attn_dense need. */
+size_t sa_attn_workspace_bytes(const sa_params* p);
+
+/*
+ * sa_attn_sparse -- block-sparse attention forward over a route.
+ *
+ * For every query token t of block i (head h, batch b), over the valid key
+ * tokens u of the key blocks listed for row (b, h, i):
+ *   l_u = softmax_scale * q_t . k_u,   a_u = exp(l_u - max l) / sum exp(.),
+ *   o_t = sum_u a_u v_u,              lse_t = max l + log sum exp(l - max l).
+ * Only the listed K/V blocks are read. A row with an empty list gives o = 0
+ * and lse = -inf.
+ *
+ * Precision: Q.K^T is a bf16 x bf16 product with fp32 accumulation; the
+ * softmax is fp32; the P.V product takes P and V in fp16 (V is repacked once
+ * per call into the workspace) with fp32 accumulation; o is rounded once to
+ * bf16. |v| must be <= 65504 (else SA_DEV_RANGE).
+ *
+ * q, k, v    device bf16 [B, S, H, D] (strides in p); not modified.
+ * row_ptr,   device int32 CSR as written by sa_route (ascending, unique
+ * col_idx    entries in [0, Nb)); rows that break this raise SA_DEV_BAD_ROUTE
+ *            and are skipped.
+ * o          device bf16 [B, S, H, D] (o_stride); rows >= S are not written.
+ * lse        device fp32 [B, H, S] (natural log), or NULL.
+ * workspace  device scratch of sa_attn_workspace_bytes(p) bytes, 256-byte
+ *            aligned.
+ */
+sa_status sa_attn_sparse(const sa_params* p, const void* q, const void* k,
+                         const void* v, const int32_t* row_ptr,
+                         const int32_t* col_idx, void* o, float* lse,
+                         void* workspace, size_t ws_bytes, int32_t* dev_status,
+                         void* stream);
+
+/*
+ * sa_attn_dense -- the same forward with every key block attended (density
+ * 100%), as the pages run for the first denoising steps and the first layers
+ * (Sol-Engine H3-DataCenter release page, policy paragraph). Arguments as in
+ * sa_attn_sparse, without the route.
+ */
+sa_status sa_attn_dense(const sa_params* p, const void* q, const void* k,
+                        const void* v, void* o, float* lse, void* workspace,
+                        size_t ws_bytes, int32_t* dev_status, void* stream);
+
+/*
+ * sa_forward_host -- one whole layer from host memory: copies q, k, v
+ * (host, pinned for asynchronous copies) to the device buffers, routes,
+ * attends, and copies o (and lse if both lse pointers are non-NULL) back,
+ * all on `stream`, then returns without synchronising. Every device buffer
+ * is the caller's, sized as for sa_route / sa_attn_sparse, with q_dev, k_dev,
+ * v_dev, o_dev laid out with the strides in p and *_host contiguous copies
+ * of the same [B, S, H, D] extents (the strides in p must then describe a
+ * contiguous tensor). The route workspace and the attention workspace may be
+ * the same buffer if it is large enough for both.
+ */
+sa_status sa_forward_host(const sa_params* p, const void* q_host,
+                          const void* k_host, const void* v_host, void* o_host,
+                          float* lse_host, void* q_dev, void* k_dev,
+                          void* v_dev, void* o_dev, float* lse_dev,
+                          int32_t* row_ptr, int32_t* col_idx, int64_t col_cap,
+                          void* workspace, size_t ws_bytes,
+                          int32_t* dev_status, void* stream);
+
+/* Decodes *dev_status bits into the most severe sa_status (SA_OK if 0). */
+sa_status sa_dev_status_decode(int32_t dev_status);
+
+/* A static, NUL-terminated name of the status. */
+const char* sa_status_string(sa_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SA_GB300_H */

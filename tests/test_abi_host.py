@@ -1,0 +1,121 @@
+"""The C ABI on the host, without a GPU: the library builds and loads, exports
+every function include/sa.h declares, sizes its buffers, and rejects bad
+arguments before it would touch a device."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from helpers import lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def sa():
+    return lib()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "sa.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(sa_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declarations_are_all_exported(sa):
+    names = declared_functions()
+    assert len(names) >= 12
+    L = sa.load_library()
+    for n in names:
+        assert hasattr(L, n), n
+    assert sorted(sa.EXPORTS) == names
+
+
+def params(sa, B=1, S=38247, H=56, D=128, P=951, tau=1.0):
+    p = sa.sa_params()
+    sa.load_library().sa_params_init(ctypes.byref(p), B, S, H, D, P, tau)
+    return p
+
+
+def test_sizes(sa):
+    L = sa.load_library()
+    p = params(sa)
+    assert L.sa_num_blocks(ctypes.byref(p)) == 598
+    assert L.sa_route_rows(ctypes.byref(p)) == 56 * 598
+    assert L.sa_route_max_nnz(ctypes.byref(p)) == 56 * 598 * 598
+    assert L.sa_attn_workspace_bytes(ctypes.byref(p)) == 56 * 128 * 38248 * 2
+    assert L.sa_route_workspace_bytes(ctypes.byref(p)) > 56 * 598 * 598 * 4
+    p1 = params(sa, S=1, H=1, D=64, P=0)
+    assert L.sa_num_blocks(ctypes.byref(p1)) == 1
+
+
+@pytest.mark.parametrize("field,value,code", [
+    ("D", 96, 2), ("D", 0, 1), ("block", 32, 1), ("S", 0, 1), ("prefix_len", -1, 1),
+    ("prefix_len", 40000, 1), ("tau", -1.0, 1), ("tau", float("inf"), 1), ("H", 0, 1),
+    ("softmax_scale", float("nan"), 1),
+])
+def test_bad_params_rejected_before_launch(sa, field, value, code):
+    L = sa.load_library()
+    p = params(sa)
+    setattr(p, field, value)
+    dummy = ctypes.c_void_p(256)
+    assert L.sa_route(ctypes.byref(p), dummy, dummy, dummy, dummy, 10, dummy, 1 << 40,
+                      None, None) == code
+    assert L.sa_attn_dense(ctypes.byref(p), dummy, dummy, dummy, dummy, None, dummy, 1 << 40,
+                           None, None) == code
+    assert L.sa_route_workspace_bytes(ctypes.byref(p)) == 0
+
+
+def test_null_and_misaligned_pointers_rejected(sa):
+    L = sa.load_library()
+    p = params(sa)
+    a = ctypes.c_void_p(4096)
+    assert L.sa_route(ctypes.byref(p), None, a, a, a, 10, a, 1 << 40, None, None) == 1
+    assert L.sa_route(ctypes.byref(p), ctypes.c_void_p(4098), a, a, a, 10, a, 1 << 40,
+                      None, None) == 1
+    assert L.sa_route(ctypes.byref(p), a, a, a, a, 10, ctypes.c_void_p(4096 + 16), 1 << 40,
+                      None, None) == 1  # workspace must be 256-byte aligned
+    assert L.sa_attn_sparse(ctypes.byref(p), a, a, a, None, a, a, None, a, 1 << 40,
+                            None, None) == 1
+    assert L.sa_route(None, a, a, a, a, 10, a, 1 << 40, None, None) == 1
+
+
+def test_small_workspace_and_bad_strides(sa):
+    L = sa.load_library()
+    p = params(sa)
+    a = ctypes.c_void_p(4096)
+    need = L.sa_route_workspace_bytes(ctypes.byref(p))
+    assert L.sa_route(ctypes.byref(p), a, a, a, a, 10, a, need - 1, None, None) == 3
+    need = L.sa_attn_workspace_bytes(ctypes.byref(p))
+    assert L.sa_attn_dense(ctypes.byref(p), a, a, a, a, None, a, need - 1, None, None) == 3
+    p.k_stride[1] = 7168 + 4   # not a multiple of 8 elements
+    assert L.sa_route(ctypes.byref(p), a, a, a, a, 10, a, 1 << 40, None, None) == 1
+
+
+def test_forward_host_requires_contiguous_layout(sa):
+    L = sa.load_library()
+    p = params(sa)
+    p.q_stride[2] = 256
+    a = ctypes.c_void_p(4096)
+    args = [a] * 12
+    assert L.sa_forward_host(ctypes.byref(p), *args, 10, a, 1 << 40, None, None) == 1
+
+
+def test_status_strings_and_decode(sa):
+    L = sa.load_library()
+    assert L.sa_status_string(0) == b"SA_OK"
+    assert L.sa_status_string(5) == b"SA_ERR_TIMEOUT"
+    assert L.sa_dev_status_decode(0) == 0
+    assert L.sa_dev_status_decode(sa.SA_DEV_TIMEOUT | sa.SA_DEV_CAPACITY) == 5
+    assert L.sa_dev_status_decode(sa.SA_DEV_CAPACITY) == 3
+
+
+def test_binding_refuses_cpu_tensors(sa):
+    import torch
+    q = torch.zeros((1, 64, 1, 64), dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        sa.sa_route(q, q, 0, 1.0)
+    with pytest.raises(ValueError):
+        sa.sa_attn_dense(q, q, q)

@@ -1,0 +1,321 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+Routing must give the oracle's kept sets exactly (ties excepted); attention
+must match within the tolerances in ``helpers``. Small shapes run in full and
+cover the ragged and degenerate cases; the release and long shapes run in the
+launch configuration the benchmark times, checked on a seeded sample of
+(head, query block) pairs that always includes the first block, the block
+holding the end of the prefix, and the ragged tail.
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sa_inputs
+from helpers import (L2_TOL, MAXABS_TOL, compare_route, f32, gather_rows, lib, lse_ok,
+                     out_errors, ref_rows, sample_items, to_np)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def sa():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return lib()
+
+
+def dev(*ts):
+    return [t.cuda() for t in ts]
+
+
+def new_status():
+    return torch.zeros(1, dtype=torch.int32, device="cuda")
+
+
+def gpu_route(sa, q, k, P, tau, scale=0.0):
+    st = new_status()
+    qd, kd = dev(q, k)
+    rp, ci = sa.sa_route(qd, kd, P, tau, scale, dev_status=st)
+    torch.cuda.synchronize()
+    return to_np(rp).astype(np.int64), to_np(ci).astype(np.int64), int(st.item())
+
+
+def gpu_attn(sa, q, k, v, row_ptr=None, col_idx=None, scale=0.0):
+    st = new_status()
+    qd, kd, vd = dev(q, k, v)
+    if row_ptr is None:
+        o, lse = sa.sa_attn_dense(qd, kd, vd, scale, dev_status=st)
+    else:
+        rp = torch.as_tensor(np.asarray(row_ptr), dtype=torch.int32, device="cuda")
+        ci = torch.as_tensor(np.asarray(col_idx), dtype=torch.int32, device="cuda")
+        o, lse = sa.sa_attn_sparse(qd, kd, vd, rp, ci, scale, dev_status=st)
+    torch.cuda.synchronize()
+    return to_np(o), to_np(lse), int(st.item())
+
+
+def check_route(sa, q, k, P, tau, scale=0.0):
+    B, S, H, D = q.shape
+    Nb = oracle.num_blocks(S)
+    ref = oracle.route_ref(q, k, P, f32(tau), scale=f32(scale) if scale else None)
+    rp, ci, st = gpu_route(sa, q, k, P, tau, scale)
+    assert st == 0, f"device status {st:#x}"
+    assert rp[-1] <= len(ci)
+    bad, ties = compare_route(rp, ci[:rp[-1]], ref, B, H, Nb)
+    assert bad == 0, f"{bad} routing decisions differ outside ties ({ties} ties)"
+    return ref, rp, ci
+
+
+def check_attn_full(sa, q, k, v, rp, ci, scale=0.0):
+    o, lse, st = gpu_attn(sa, q, k, v, rp, ci, scale)
+    assert st == 0, f"device status {st:#x}"
+    o_ref, lse_ref = oracle.attn_ref(q, k, v, rp, ci, scale=f32(scale) if scale else None)
+    l2, mx, l2_64 = out_errors(o, o_ref)
+    assert l2 <= L2_TOL and mx <= MAXABS_TOL, (l2, mx, l2_64)
+    assert lse_ok(lse, lse_ref)
+    return o, lse
+
+
+# ------------------------------------------------------------ small shapes --
+
+SMALL = [  # (S, H, D, P, tau)
+    (1, 2, 64, 0, 1.0),
+    (50, 2, 128, 50, 1.0),
+    (64, 3, 64, 1, 1.0),
+    (65, 2, 128, 0, 1.0),
+    (130, 2, 64, 64, 1.0),
+    (200, 1, 128, 0, 0.0),
+    (383, 2, 128, 100, 1.0),
+    (640, 2, 64, 0, 1.5),
+    (1000, 2, 128, 951, 1.0),
+]
+
+
+@pytest.mark.parametrize("S,H,D,P,tau", SMALL)
+def test_small_shapes_route_and_attention(sa, S, H, D, P, tau):
+    q, k, v = sa_inputs.random_small(S, H, D, seed=S + H + D)
+    ref, rp, ci = check_route(sa, q, k, P, tau)
+    check_attn_full(sa, q, k, v, ref["row_ptr"], ref["col_idx"])
+
+
+def test_dense_small_against_dense_oracle(sa):
+    q, k, v = sa_inputs.random_small(333, 3, 128, seed=21)
+    o, lse, st = gpu_attn(sa, q, k, v)
+    assert st == 0
+    o_ref, lse_ref = oracle.attn_dense_ref(q, k, v)
+    l2, mx, _ = out_errors(o, o_ref)
+    assert l2 <= L2_TOL and mx <= MAXABS_TOL and lse_ok(lse, lse_ref)
+
+
+def test_custom_softmax_scale(sa):
+    q, k, v = sa_inputs.random_small(300, 2, 64, seed=4)
+    ref, rp, ci = check_route(sa, q, k, 64, 1.0, scale=0.3)
+    check_attn_full(sa, q, k, v, ref["row_ptr"], ref["col_idx"], scale=0.3)
+
+
+def test_batch_and_strided_views(sa):
+    # B = 2, heads 1..3 of a 5-head buffer: non-contiguous b/s/h strides
+    g = torch.Generator().manual_seed(8)
+    big = [torch.randn((2, 300, 5, 128), generator=g).to(torch.bfloat16) for _ in range(3)]
+    q, k, v = (t[:, :, 1:4, :] for t in big)
+    ref = oracle.route_ref(q, k, 70, 1.0)
+    qd, kd, vd = (t.cuda()[:, :, 1:4, :] for t in big)
+    assert not qd.is_contiguous()
+    st = new_status()
+    rp, ci = sa.sa_route(qd, kd, 70, 1.0, dev_status=st)
+    o = torch.empty((2, 300, 3, 128), dtype=torch.bfloat16, device="cuda")
+    o, lse = sa.sa_attn_sparse(qd, kd, vd, rp, ci, o=o, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    rpn, cin = to_np(rp).astype(np.int64), to_np(ci).astype(np.int64)
+    bad, _ = compare_route(rpn, cin[:rpn[-1]], ref, 2, 3, 5)
+    assert bad == 0
+    o_ref, lse_ref = oracle.attn_ref(q, k, v, rpn, cin)
+    l2, mx, _ = out_errors(to_np(o), o_ref)
+    assert l2 <= L2_TOL and mx <= MAXABS_TOL and lse_ok(to_np(lse), lse_ref)
+
+
+def test_empty_rows_give_zero_output_and_neg_inf_lse(sa):
+    S, H, D = 256, 1, 64
+    q, k, v = sa_inputs.random_small(S, H, D, seed=30)
+    rows = [[0, 2], [], [1, 2, 3], []]
+    rp = np.concatenate([[0], np.cumsum([len(r) for r in rows])])
+    ci = np.array([j for r in rows for j in r])
+    o, lse, st = gpu_attn(sa, q, k, v, rp, ci)
+    assert st == 0
+    o_ref, lse_ref = oracle.attn_ref(q, k, v, rp, ci)
+    assert np.all(o[0, 64:128] == 0) and np.all(np.isneginf(lse[0, 0, 64:128]))
+    assert np.all(o[0, 192:256] == 0) and np.all(np.isneginf(lse[0, 0, 192:256]))
+    l2, mx, _ = out_errors(o, o_ref)
+    assert l2 <= L2_TOL and mx <= MAXABS_TOL and lse_ok(lse, lse_ref)
+
+
+# ------------------------------------------------------------ Tiny / Mid --
+
+@pytest.fixture(scope="module")
+def tiny():
+    return sa_inputs.make_inputs("tiny")
+
+
+@pytest.fixture(scope="module")
+def mid():
+    return sa_inputs.make_inputs("mid")
+
+
+def test_tiny_route_bitexact_and_full_attention(sa, tiny):
+    cfg, q, k, v = tiny
+    ref, rp, ci = check_route(sa, q, k, cfg.P, cfg.tau)
+    assert abs(oracle.block_density(ref["kept"]) - 0.25) <= 0.01
+    # the attention the CUDA path computes over its own route
+    check_attn_full(sa, q, k, v, rp[: len(rp)], ci[: rp[-1]])
+
+
+def test_mid_route_bitexact_and_full_attention(sa, mid):
+    cfg, q, k, v = mid
+    ref, rp, ci = check_route(sa, q, k, cfg.P, cfg.tau)
+    assert 0.18 <= oracle.block_density(ref["kept"]) <= 0.22
+    check_attn_full(sa, q, k, v, ref["row_ptr"], ref["col_idx"])
+
+
+def test_tau_zero_sparse_equals_dense_bitwise(sa, mid):
+    cfg, q, k, v = mid
+    rp, ci, st = gpu_route(sa, q, k, cfg.P, 0.0)
+    assert st == 0 and rp[-1] == cfg.H * cfg.Nb * cfg.Nb
+    o_s, l_s, _ = gpu_attn(sa, q, k, v, rp, ci[: rp[-1]])
+    o_d, l_d, _ = gpu_attn(sa, q, k, v)
+    assert np.array_equal(o_s, o_d) and np.array_equal(l_s, l_d)
+
+
+def test_unselected_blocks_are_never_read(sa, mid):
+    # perturbing K/V of a key block changes no output row whose route skips it
+    cfg, q, k, v = mid
+    ref = oracle.route_ref(q, k, cfg.P, f32(cfg.tau))
+    rp, ci = ref["row_ptr"], ref["col_idx"]
+    o0, l0, _ = gpu_attn(sa, q, k, v, rp, ci)
+    h, jstar = 3, 77
+    k2, v2 = k.clone(), v.clone()
+    k2[0, 64 * jstar:64 * jstar + 64, h] = 7.0
+    v2[0, 64 * jstar:64 * jstar + 64, h] = -5.0
+    o1, l1, _ = gpu_attn(sa, q, k2, v2, rp, ci)
+    kept = ref["kept"][0, h]
+    untouched = [i for i in range(cfg.Nb) if not kept[i, jstar]]
+    touched = [i for i in range(cfg.Nb) if kept[i, jstar]]
+    assert untouched and touched
+    for i in untouched:
+        sl = slice(64 * i, 64 * i + 64)
+        assert np.array_equal(o0[0, sl, h], o1[0, sl, h]), i
+        assert np.array_equal(l0[0, h, sl], l1[0, h, sl]), i
+    assert any(not np.array_equal(o0[0, 64 * i:64 * i + 64, h], o1[0, 64 * i:64 * i + 64, h])
+               for i in touched)
+    other = [hh for hh in range(cfg.H) if hh != h]
+    assert np.array_equal(o0[:, :, other], o1[:, :, other])
+
+
+# -------------------------------------------------------- device statuses --
+
+def test_capacity_overflow_is_reported(sa):
+    q, k, _ = sa_inputs.random_small(512, 2, 64, seed=2)
+    st = new_status()
+    col_idx = torch.full((5,), -1, dtype=torch.int32, device="cuda")
+    rp, _ = sa.sa_route(q.cuda(), k.cuda(), 0, 0.0, col_idx=col_idx, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) & sa.SA_DEV_CAPACITY
+    assert int(rp[-1].item()) == 2 * 8 * 8            # row_ptr stays exact
+    assert to_np(col_idx).tolist() == [0, 1, 2, 3, 4]
+
+
+def test_bad_route_entries_are_reported_and_skipped(sa):
+    S, H, D = 256, 1, 64
+    q, k, v = sa_inputs.random_small(S, H, D, seed=31)
+    rp = np.array([0, 2, 3, 5, 6])
+    ci = np.array([0, 9, 1, 2, -3, 3])   # 9 and -3 are outside [0, 4)
+    o, lse, st = gpu_attn(sa, q, k, v, rp, ci)
+    assert st & sa.SA_DEV_BAD_ROUTE
+    good_rp = np.array([0, 1, 2, 3, 4])
+    good_ci = np.array([0, 1, 2, 3])
+    o_ref, lse_ref = oracle.attn_ref(q, k, v, good_rp, good_ci)
+    l2, mx, _ = out_errors(o, o_ref)
+    assert l2 <= L2_TOL and mx <= MAXABS_TOL
+
+
+def test_v_outside_fp16_range_is_reported(sa):
+    q, k, v = sa_inputs.random_small(128, 1, 64, seed=3)
+    v[0, 5, 0, 3] = 1.0e5
+    _, _, st = gpu_attn(sa, q, k, v)
+    assert st & sa.SA_DEV_RANGE
+
+
+def test_forward_host_matches_device_calls(sa):
+    cfg, q, k, v = sa_inputs.make_inputs("tiny")
+    bufs = sa.alloc_layer_buffers(1, cfg.S, cfg.H, cfg.D)
+    qh, kh, vh = (t.contiguous().pin_memory() for t in (q, k, v))
+    o_host = sa.sa_forward_host(qh, kh, vh, cfg.P, cfg.tau, bufs=bufs)
+    torch.cuda.synchronize()
+    assert int(bufs["status"].item()) == 0
+    rp, ci, _ = gpu_route(sa, q, k, cfg.P, cfg.tau)
+    o_dev, _, _ = gpu_attn(sa, q, k, v, rp, ci[: rp[-1]])
+    assert np.array_equal(to_np(o_host), o_dev)
+
+
+# --------------------------------------------- release / dense / long shapes --
+
+@pytest.fixture(scope="module")
+def release():
+    cfg, q, k, v = sa_inputs.make_inputs("release")
+    return cfg, q, k, v
+
+
+def _sampled_attention_check(sa, cfg, q, k, v, rp, ci, seed, dense=False):
+    qd, kd, vd = dev(q, k, v)
+    st = new_status()
+    if dense:
+        o, lse = sa.sa_attn_dense(qd, kd, vd, dev_status=st)
+    else:
+        rpd = torch.as_tensor(rp, dtype=torch.int32, device="cuda")
+        cid = torch.as_tensor(ci, dtype=torch.int32, device="cuda")
+        o, lse = sa.sa_attn_sparse(qd, kd, vd, rpd, cid, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    Nb, n_sink = cfg.Nb, (cfg.P + 63) // 64
+    items = sample_items(1, cfg.H, Nb, 8, 16, seed, must=(0, n_sink - 1, Nb - 2, Nb - 1))
+    if dense:
+        ref = oracle.attn_dense_ref(q, k, v, items=items)
+    else:
+        ref = oracle.attn_ref(q, k, v, rp, ci, items=items)
+    o_np = o.float().cpu().double().numpy()
+    lse_np = lse.cpu().double().numpy()
+    og, lg = gather_rows(o_np, lse_np, items, cfg.S)
+    orf, lrf = ref_rows(ref, items)
+    l2, mx, l2_64 = out_errors(og, orf)
+    assert l2 <= L2_TOL and mx <= MAXABS_TOL, (l2, mx, l2_64)
+    assert lse_ok(lg, lrf)
+
+
+def test_release_route_bitexact(sa, release):
+    cfg, q, k, v = release
+    ref, rp, ci = check_route(sa, q, k, cfg.P, cfg.tau)
+    d = oracle.block_density(ref["kept"])
+    assert 0.18 <= d <= 0.20, d
+
+
+def test_release_attention_sampled(sa, release):
+    cfg, q, k, v = release
+    ref = oracle.route_ref(q, k, cfg.P, f32(cfg.tau))
+    _sampled_attention_check(sa, cfg, q, k, v, ref["row_ptr"], ref["col_idx"], seed=1)
+
+
+def test_dense_release_sampled(sa, release):
+    cfg, q, k, v = release
+    _sampled_attention_check(sa, cfg, q, k, v, None, None, seed=2, dense=True)
+
+
+def test_long_route_bitexact_and_attention_sampled(sa):
+    cfg, q, k, v = sa_inputs.make_inputs("long")
+    ref, rp, ci = check_route(sa, q, k, cfg.P, cfg.tau)
+    d = oracle.block_density(ref["kept"])
+    assert 0.12 <= d <= 0.15, d
+    _sampled_attention_check(sa, cfg, q, k, v, ref["row_ptr"], ref["col_idx"], seed=3)

@@ -1,0 +1,385 @@
+"""Benchmark of one routed block-sparse attention layer on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload release|long|dense|mid|tiny] [--no-e2e] [--no-cpu]
+
+One step = the whole hot path on one batch of synthetic input already in
+HBM: sa_route (pool, score, select, recheck, scan, emit) then sa_attn_sparse
+(V repack + attention), at the release shape S=38,247, H=56, D=128, prefix
+951, tau=1.0 (~19% block density). The metric is effective TFLOP/s on the
+routed pairs: FLOPs = 4 * D * sum over routed (query block, key block) pairs
+of (valid queries) x (valid keys), divided by the step time.
+
+Inputs (Q, K, V, O = 2.19 GB) are larger than the 129 MB L2, so no flush runs
+between steps. Steps are timed with CUDA events on the stream the kernels are
+launched on, W untimed warm-up steps first, with a barrier and
+torch.cuda.synchronize() on both sides; for N > 1 each rank (one GPU each,
+torchrun) runs an independent replica of the layer (the path has no exchange
+step) and the max time over ranks is used.
+
+--impl reference times the CPU oracle (the reference arm: no code exists to
+run for this method) on a bounded sample of the same workload and scales it
+to a whole layer.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import sa_inputs  # noqa: E402
+
+METRIC = "ms/layer and effective TFLOP/s (% of GB300 bf16 peak) at S=38,247, ~18% density"
+UNIT = "TFLOP/s"
+KERNELS_PER_STEP = 8  # pool, score, select, recheck, scan, emit, pack_v, attention
+
+# DRAM traffic of one attention-kernel launch at the release workload, from
+# the ncu capture summarised under profiles/, valid only for the attn.cu it
+# was taken on (sha256 prefix).
+ATTN_TRAFFIC = {"bytes": None, "attn_cu_sha256": None}
+
+
+def file_sha(path):
+    return hashlib.sha256(open(path, "rb").read()).hexdigest()
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d.get("bf16_tflops"), d.get("bf16_tflops_sustained"), d.get("hbm_gbs"), "measured"
+    return 1900.0, 1700.0, 6800.0, "fallback"
+
+
+# ---------------------------------------------------------------- helpers --
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def reduce_max(x: float, world: int, device=None) -> float:
+    """Max of a per-rank scalar over all ranks (identity for one rank)."""
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.gpu)],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9 and parts[1].isdigit():
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        reasons = sorted({self.REASONS[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        sm = [int(r[1]) for r in rows]
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return 0.0
+
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": int(rows[0][2]),
+                "power_w_max": max(num(r[3]) for r in rows), "samples": len(rows),
+                "reasons": reasons}
+
+
+# ------------------------------------------------------------- our arm -----
+
+def routed_flops(row_ptr: np.ndarray, col_idx: np.ndarray, B, H, S, D) -> int:
+    """4 * D * sum over routed pairs of valid queries x valid keys."""
+    Nb = (S + 63) // 64
+    counts = np.minimum(64, S - 64 * np.arange(Nb))
+    cs = np.concatenate([[0], np.cumsum(counts[col_idx])])
+    per_row = cs[row_ptr[1:]] - cs[row_ptr[:-1]]
+    ni = counts[np.arange(B * H * Nb) % Nb]
+    return int(4 * D * int((ni * per_row).sum()))
+
+
+def run_ours(args):
+    import block_sparse_attention_sa_gb300 as sa
+    from block_sparse_attention_sa_gb300 import build as _build
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0:
+        _build.build()
+    barrier(world)
+    sa.load_library()
+
+    cfg = sa_inputs.get_config(args.workload)
+    q, k, v = sa_inputs.make_qkv(cfg)
+    B, S, H, D = q.shape
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    bufs = sa.alloc_layer_buffers(B, S, H, D, device=dev)
+    ws, status = bufs["ws"], bufs["status"]
+    o, lse, rp_buf, ci_buf = bufs["o"], bufs["lse"], bufs["row_ptr"], bufs["col_idx"]
+    stream = torch.cuda.current_stream(dev)
+    dense = cfg.dense
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        if not dense:
+            sa.sa_route(qd, kd, cfg.P, cfg.tau, row_ptr=rp_buf, col_idx=ci_buf, workspace=ws,
+                        dev_status=status)
+        if ev is not None:
+            ev[1].record(stream)
+        if dense:
+            sa.sa_attn_dense(qd, kd, vd, o=o, lse=lse, workspace=ws, dev_status=status)
+        else:
+            sa.sa_attn_sparse(qd, kd, vd, rp_buf, ci_buf, o=o, lse=lse, workspace=ws,
+                              dev_status=status)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    sa.check_dev_status(status, "bench warm-up")
+    Nb = cfg.Nb
+    if dense:
+        row_ptr = np.arange(B * H * Nb + 1, dtype=np.int64) * Nb
+        col_idx = np.tile(np.arange(Nb), B * H * Nb)
+    else:
+        row_ptr = rp_buf.cpu().numpy().astype(np.int64)
+        col_idx = ci_buf[: int(row_ptr[-1])].cpu().numpy().astype(np.int64)
+    flops = routed_flops(row_ptr, col_idx, B, H, S, D)
+    density = float(row_ptr[-1]) / (B * H * Nb * Nb)
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        start.record(stream)
+        for i in range(args.steps):
+            step(evs[i])
+        end.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    sa.check_dev_status(status, "bench")
+    total_ms = reduce_max(start.elapsed_time(end), world, dev)
+    route_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    attn_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    ms_step = total_ms / args.steps
+    value = world * flops / (ms_step * 1e-3) / 1e12
+    attn_avg = statistics.mean(attn_ms)
+    burst, sustained, _, peak_src = measured_peaks()
+    long_region = total_ms > 1000.0
+    peak = sustained if long_region else burst
+    achieved = flops / (attn_avg * 1e-3) / 1e12
+    sha = file_sha(os.path.join(ROOT, "block_sparse_attention_sa_gb300", "csrc", "attn.cu"))
+    traffic = (ATTN_TRAFFIC["bytes"]
+               if ATTN_TRAFFIC["attn_cu_sha256"] and sha.startswith(ATTN_TRAFFIC["attn_cu_sha256"])
+               else None)
+
+    e2e = None if args.no_e2e else run_e2e(sa, cfg, q, k, v, bufs, flops, args, world, dev, stream)
+
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; stands in for the model's activations)",
+        "config": {"workload": cfg.name, "B": B, "S": S, "H": H, "D": D, "prefix": cfg.P,
+                   "tau": cfg.tau, "block": 64, "density": round(density, 5),
+                   "routed_tflop_per_layer": round(flops / 1e12, 4),
+                   "ms_route": round(statistics.mean(route_ms), 4),
+                   "ms_attn": round(attn_avg, 4),
+                   "l2": "inputs larger than L2 (Q/K/V/O %.2f GB), no flush" % (4 * q.numel() * 2 / 1e9),
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": {"bound": "tensor", "kernel": "sa_attn_sparse (V repack + attention)",
+                     "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak, 4),
+                     "peak_kind": f"{'sustained' if long_region else 'burst'} bf16, {peak_src}",
+                     "traffic": traffic},
+        "gpu_launches": KERNELS_PER_STEP * args.steps,
+        "e2e": e2e,
+        "clocks": clk.summary(),
+    }
+    if world == 1 and not args.no_cpu and rank == 0:
+        result["cpu_baseline"] = cpu_baseline(cfg, q, k, v, flops, budget_s=15.0)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_e2e(sa, cfg, q, k, v, bufs, flops, args, world, dev, stream):
+    """The same layer through sa_forward_host: pinned host Q/K/V in, host O out,
+    copies inside the timed region."""
+    qh, kh, vh = (t.contiguous().pin_memory() for t in (q, k, v))
+    oh = torch.empty_like(qh, pin_memory=True)
+    steps = max(3, min(args.steps, 10))
+    for _ in range(2):
+        sa.sa_forward_host(qh, kh, vh, cfg.P, cfg.tau, bufs=bufs, o_host=oh)
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    s.record(stream)
+    for _ in range(steps):
+        sa.sa_forward_host(qh, kh, vh, cfg.P, cfg.tau, bufs=bufs, o_host=oh)
+    e.record(stream)
+    torch.cuda.synchronize()
+    ms = reduce_max(s.elapsed_time(e), world, dev) / steps
+    nbytes = q.numel() * 2
+    return {"value": round(world * flops / (ms * 1e-3) / 1e12, 2), "unit": UNIT,
+            "ms_per_step": round(ms, 4), "h2d_bytes_per_step": 3 * nbytes,
+            "d2h_bytes_per_step": nbytes}
+
+
+# ------------------------------------------------------- the CPU oracle ----
+
+def cpu_baseline(cfg, q, k, v, flops, budget_s=15.0, seed=0):
+    """Time the oracle on a bounded sample of the layer and scale to a whole
+    layer: the route of one head in full, plus as many query blocks of that
+    head as fit in ``budget_s`` (at least 4), extrapolated linearly to all
+    heads and blocks."""
+    import oracle
+
+    B, S, H, D = q.shape
+    Nb = cfg.Nb
+    h = seed % H
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    qs, ks, vs = (t[:, :, h:h + 1].contiguous() for t in (q, k, v))
+    t0 = time.perf_counter()
+    r = oracle.route_ref(qs, ks, cfg.P, float(np.float32(cfg.tau)))
+    t_route = time.perf_counter() - t0
+    order = np.random.default_rng(seed).permutation(Nb)
+    t_attn, n_done = 0.0, 0
+    while n_done < Nb and (n_done < 4 or t_attn < budget_s):
+        i = int(order[n_done])
+        t0 = time.perf_counter()
+        oracle.attn_ref(qs, ks, vs, r["row_ptr"], r["col_idx"], items=[(0, 0, i)])
+        t_attn += time.perf_counter() - t0
+        n_done += 1
+    layer_s = t_route * B * H + t_attn * (B * H * Nb / n_done)
+    return {"value": round(flops / layer_s / 1e12, 6), "unit": UNIT, "cores": cores,
+            "kind": "oracle",
+            "sample": f"head {h}: full route ({t_route:.1f} s) + {n_done} query blocks of "
+                      f"attention ({t_attn:.1f} s); extrapolated linearly to {B * H} heads x "
+                      f"{Nb} blocks = {layer_s:.0f} s per layer"}
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    cfg = sa_inputs.get_config(args.workload)
+    q, k, v = sa_inputs.make_qkv(cfg)
+    B, S, H, D = q.shape
+    import oracle
+    # the layer's routed FLOPs from the oracle's own route
+    ref = oracle.route_ref(q, k, cfg.P, float(np.float32(cfg.tau)))
+    flops = routed_flops(ref["row_ptr"], ref["col_idx"], B, H, S, D)
+    del ref
+    for w in range(args.warmup):
+        cpu_baseline(cfg, q, k, v, flops, budget_s=1.0, seed=w)
+    vals = [cpu_baseline(cfg, q, k, v, flops, budget_s=5.0, seed=100 + s)
+            for s in range(args.steps)]
+    value = statistics.mean(c["value"] for c in vals)
+    ms = flops / (value * 1e12) * 1e3
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms, 1), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+        "config": {"workload": cfg.name, "B": B, "S": S, "H": H, "D": D, "prefix": cfg.P,
+                   "tau": cfg.tau},
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": vals[0]["cores"],
+                         "kind": "oracle", "sample": vals[-1]["sample"]},
+        "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="release", choices=sorted(sa_inputs.CONFIGS))
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

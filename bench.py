@@ -176,7 +176,7 @@ def run_ours(args):
     barrier(world)
     sa.load_library()
 
-    cfg = sa_inputs.get_config(args.workload)
+    cfg = sa_inputs.get_config(args.workload, **({"H": args.heads} if args.heads else {}))
     q, k, v = sa_inputs.make_qkv(cfg)
     B, S, H, D = q.shape
     qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
@@ -371,6 +371,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="release", choices=sorted(sa_inputs.CONFIGS))
+    ap.add_argument("--heads", type=int, default=0,
+                    help="override H (smaller captures for profiling)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     args = ap.parse_args()

@@ -41,7 +41,9 @@ EXPORTS = (
     "sa_params_init", "sa_num_blocks", "sa_route_rows", "sa_route_max_nnz",
     "sa_route_workspace_bytes", "sa_route", "sa_attn_workspace_bytes", "sa_attn_sparse",
     "sa_attn_dense", "sa_forward_host", "sa_dev_status_decode", "sa_status_string",
+    "sa_route_static",
 )
+SA_ROUTE_STATIC_WS_BYTES = 32 << 20
 
 
 class SaError(RuntimeError):
@@ -85,6 +87,7 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         "sa_route_workspace_bytes": (sz, [P]),
         "sa_attn_workspace_bytes": (sz, [P]),
         "sa_route": (ctypes.c_int, [P, vp, vp, vp, vp, i64, vp, sz, vp, vp]),
+        "sa_route_static": (ctypes.c_int, [P, vp, vp, vp, vp, i64, vp, vp]),
         "sa_attn_sparse": (ctypes.c_int, [P, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp]),
         "sa_attn_dense": (ctypes.c_int, [P, vp, vp, vp, vp, vp, vp, sz, vp, vp]),
         "sa_forward_host": (ctypes.c_int, [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i64,

@@ -124,6 +124,40 @@ sa_status sa_route(const sa_params* p, const void* q, const void* k,
                    void* workspace, size_t ws_bytes, int32_t* dev_status,
                    void* stream);
 
+/* Size of the library-owned device scratch array sa_route_static runs on. */
+#define SA_ROUTE_STATIC_WS_BYTES (32u << 20) /* 32 MiB */
+
+/*
+ * sa_route_static -- sa_route for callers that cannot allocate device
+ * memory. The pages have no counterpart to this entry point; it exists for
+ * callers such as a plugin inside an inference engine that has already
+ * reserved all of HBM for its own pool, or code on a latency-critical path
+ * where a cudaMalloc would synchronise the device.
+ *
+ * It computes exactly what sa_route computes (same kernels, same result) but
+ * takes no workspace: the scratch lives in a fixed device array of
+ * SA_ROUTE_STATIC_WS_BYTES inside the library, which every GPU that loads
+ * the library holds until the process exits. It allocates nothing and frees
+ * nothing. The caller still passes q, k, row_ptr, col_idx (as for sa_route).
+ *
+ * Limits and behaviour:
+ *  - Shapes whose sa_route_workspace_bytes(p) exceeds SA_ROUTE_STATIC_WS_BYTES
+ *    are rejected with SA_ERR_CAPACITY before anything is launched (for
+ *    example S = 38,247 fits up to 8 heads of D = 128, S = 8,192 up to 64).
+ *  - The first call on each device, made with that device current, looks up
+ *    the array's device address and caches it; make that first call before
+ *    any stream capture.
+ *  - Every call on a device uses the same array and finds the previous call's
+ *    contents there; what must start at zero is cleared by each call. Calls
+ *    whose work overlaps on the GPU (e.g. on two unordered streams) race on
+ *    the array and give undefined routes: order them on one stream.
+ * Errors: as sa_route, plus SA_ERR_CAPACITY for shapes beyond the limit and
+ * SA_ERR_CUDA if the array's address cannot be obtained.
+ */
+sa_status sa_route_static(const sa_params* p, const void* q, const void* k,
+                          int32_t* row_ptr, int32_t* col_idx, int64_t col_cap,
+                          int32_t* dev_status, void* stream);
+
 /* Bytes of device workspace sa_attn_sparse / sa_attn_dense need. */
 size_t sa_attn_workspace_bytes(const sa_params* p);
 

@@ -18,9 +18,11 @@
 //              lane issues every TMA load (Q once; K and V^T per step)
 //   warp  5    allocates TMEM; one lane issues every tcgen05.mma
 // Pipeline per step j: K(j) -> S[j%2] = Q K^T (bf16, fp32 in TMEM)
-//   -> softmax(j) reads S, writes P (fp16) to shared memory, rescales O
-//   in TMEM when the running max moved by more than 2^8
-//   -> O += P V (fp16, fp32 in TMEM). QK^T(j+1) overlaps softmax(j).
+//   -> softmax(j) reads S, writes P (fp16) back over the same TMEM columns,
+//   and rescales O in TMEM only when the running max moved by more than 2^8
+//   -> O += P V with P read from TMEM (fp16, fp32 accumulation). The tensor
+//   pipe runs QK^T(j+1) and PV(j) while softmax(j+1) runs; softmax waits for
+//   the previous PV only when it has to rescale O.
 // The producer alone reads the route, before the pipeline starts, so no
 // data-dependent load sits inside the pipelined loops.
 // Every wait is bounded (SA_DEV_TIMEOUT) and an aborted CTA drains its own
@@ -38,7 +40,7 @@ namespace {
 
 constexpr int BM = 128;   // query rows per tile
 constexpr int BN = 128;   // key rows per step (two key blocks)
-constexpr int KST = 2;    // K stages
+constexpr int KST = 3;    // K stages
 constexpr int VST = 2;    // V stages
 constexpr int kThreads = 192;
 constexpr int kTmemCols = 512;
@@ -55,9 +57,7 @@ struct Smem {
   static constexpr int kV = kK + KST * kKBytes;
   static constexpr int kVBytes = BN * D * 2;
   static constexpr int kVHalf = D * 128;              // one 64-key half of a V^T stage
-  static constexpr int kP = kV + VST * kVBytes;
-  static constexpr int kPBytes = BM * BN * 2;
-  static constexpr int kBar = kP + kPBytes;
+  static constexpr int kBar = kV + VST * kVBytes;
   // barriers
   static constexpr int bQFull = 0;
   static constexpr int bKFull = 1;
@@ -88,6 +88,41 @@ __device__ __forceinline__ uint32_t pack_bf162(float a, float b) {
 
 __device__ __forceinline__ void set_status(int32_t* st, int bits) {
   if (st) atomicOr(st, bits);
+}
+
+// max over 64 fp32 values (bit patterns), eight independent chains.
+__device__ __forceinline__ float max64(const uint32_t* v) {
+  float m[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) m[i] = __uint_as_float(v[i]);
+#pragma unroll
+  for (int i = 8; i < 64; ++i) m[i & 7] = fmaxf(m[i & 7], __uint_as_float(v[i]));
+#pragma unroll
+  for (int w = 4; w >= 1; w >>= 1)
+#pragma unroll
+    for (int i = 0; i < w; ++i) m[i] = fmaxf(m[i], m[i + w]);
+  return m[0];
+}
+
+// p = 2^(s * c - m) for 64 logits, packed as fp16 pairs into 32 words;
+// returns the fp32 sum of the p (eight independent chains).
+__device__ __forceinline__ float exp_pack64(const uint32_t* v, float c, float negm,
+                                            uint32_t* pk) {
+  float acc[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+#pragma unroll
+  for (int u = 0; u < 64; u += 2) {
+    const float p0 = fast_exp2(fmaf(__uint_as_float(v[u]), c, negm));
+    const float p1 = fast_exp2(fmaf(__uint_as_float(v[u + 1]), c, negm));
+    acc[(u >> 1) & 7] += p0 + p1;
+    pk[u >> 1] = pack_half2(p0, p1);
+  }
+#pragma unroll
+  for (int w = 4; w >= 1; w >>= 1)
+#pragma unroll
+    for (int i = 0; i < w; ++i) acc[i] += acc[i + w];
+  return acc[0];
 }
 
 template <int D>
@@ -272,11 +307,12 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         if (!mbar_wait(bar(L::bVFull + vs), (j / VST) & 1, abort_sig)) { ok = false; break; }
         tc_fence_after();
         const int nblk = (2 * j + 1 < n_entries) ? 2 : 1;
-        const uint32_t pa = sbase + L::kP, vb = sbase + L::kV + vs * L::kVBytes;
+        const uint32_t pa = tmem + ((j & 1) ? kColS1 : kColS0);  // P(j) over S(j)
+        const uint32_t vb = sbase + L::kV + vs * L::kVBytes;
         for (int kk = 0; kk < nblk * 4; ++kk) {
           const uint32_t kh = kk >> 2, off = (kk & 3) * 32;
-          umma_ss(tmem + kColO, sdesc_kmajor_sw128(pa + kh * L::kRegion + off),
-                  sdesc_kmajor_sw128(vb + kh * L::kVHalf + off), kIdPV, (j > 0 || kk > 0));
+          umma_ts(tmem + kColO, pa + 8 * kk, sdesc_kmajor_sw128(vb + kh * L::kVHalf + off), kIdPV,
+                  (j > 0 || kk > 0));
         }
         umma_commit(bar(L::bOReady));
         umma_commit(bar(L::bVEmpty + vs));
@@ -292,10 +328,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   } else {
     // ------------------------------------------------------------- softmax
     const int r = threadIdx.x;                 // tile row == TMEM lane
-    const int qh = r >> 6;
+    const int qh = r >> 6;                     // query block of this row (warp-uniform)
     const int t = qb0 * kBlock + r;            // query token
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
     const int last_valid = S - (Nb - 1) * kBlock;  // tokens in the last block
+    const float cl2 = a.scale_log2;
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
 
@@ -305,90 +342,79 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       const int nblk = (2 * j + 1 < n_entries) ? 2 : 1;
       const uint32_t e0 = info[2 * j];
       const uint32_t e1 = nblk == 2 ? info[2 * j + 1] : 0u;
+      const bool mem0 = (e0 >> qh) & 1u;
+      const bool mem1 = nblk == 2 && ((e1 >> qh) & 1u);
       const uint32_t s_col = (j & 1) ? kColS1 : kColS0;
 
-      float x[BN];
-      {
-        uint32_t raw[32];
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          tmem_ld32(lane_base + s_col + 32 * c, raw);
-          tmem_wait_ld();
-#pragma unroll
-          for (int u = 0; u < 32; ++u) x[32 * c + u] = __uint_as_float(raw[u]);
-        }
-        if (nblk == 2) {
-#pragma unroll
-          for (int c = 2; c < 4; ++c) {
-            tmem_ld32(lane_base + s_col + 32 * c, raw);
-            tmem_wait_ld();
-#pragma unroll
-            for (int u = 0; u < 32; ++u) x[32 * c + u] = __uint_as_float(raw[u]);
-          }
-        }
+      uint32_t sr[BN];
+      if (mem0) {
+        tmem_ld32(lane_base + s_col, sr);
+        tmem_ld32(lane_base + s_col + 32, sr + 32);
       }
-      // masks: membership of this row's query block, and the ragged tail
-      int nv[2];
-      {
-        const uint32_t ee[2] = {e0, e1};
-#pragma unroll
-        for (int kh = 0; kh < 2; ++kh) {
-          const int jk = static_cast<int>(ee[kh] >> 2);
-          const bool member = kh < nblk && ((ee[kh] >> qh) & 1u);
-          nv[kh] = member ? (jk == Nb - 1 ? last_valid : kBlock) : 0;
-        }
+      if (mem1) {
+        tmem_ld32(lane_base + s_col + 64, sr + 64);
+        tmem_ld32(lane_base + s_col + 96, sr + 96);
       }
-      float bmax = -INFINITY;
+      tmem_wait_ld();
+      // the ragged last block: keys past S weigh exactly zero
+      if (mem0 && static_cast<int>(e0 >> 2) == Nb - 1) {
 #pragma unroll
-      for (int c = 0; c < BN; ++c) {
-        const int kh = c >> 6, cc = c & 63;
-        x[c] = (cc < nv[kh]) ? x[c] * a.scale_log2 : -INFINITY;
-        bmax = fmaxf(bmax, x[c]);
+        for (int u = 0; u < 64; ++u)
+          if (u >= last_valid) sr[u] = __float_as_uint(-INFINITY);
       }
+      if (mem1 && static_cast<int>(e1 >> 2) == Nb - 1) {
+#pragma unroll
+        for (int u = 0; u < 64; ++u)
+          if (u >= last_valid) sr[64 + u] = __float_as_uint(-INFINITY);
+      }
+      float mx = -INFINITY;
+      if (mem0) mx = fmaxf(mx, max64(sr));
+      if (mem1) mx = fmaxf(mx, max64(sr + 64));
+      const float bmax = mx * cl2;           // the scale is positive: max commutes
       float m_new = m_run;
-      if (bmax > m_run + kRescaleLog2 || (m_run == -INFINITY && bmax > -INFINITY)) m_new = bmax;
-      const float alpha = (m_new == m_run) ? 1.f : exp2f(m_run - m_new);
-      float rsum = 0.f;
-      uint32_t pk[BN / 2];
+      if (bmax > m_run + kRescaleLog2) m_new = bmax;  // also the first finite block
+      const bool rescale = (m_new != m_run) && (m_run != -INFINITY);
+      const float alpha = (m_new == m_run) ? 1.f : fast_exp2(m_run - m_new);
+      const float negm = -m_new;
+      // P(j) over the consumed S(j) columns: keys 0-63 -> columns 0-31,
+      // keys 64-127 -> columns 32-63 (two fp16 per column). Each half is
+      // stored as soon as it is ready, so only 32 packed words stay live.
+      float rs = 0.f;
+      {
+        uint32_t pk[32];
+        if (mem0) rs += exp_pack64(sr, cl2, negm, pk);
+        else {
 #pragma unroll
-      for (int c = 0; c < BN; c += 2) {
-        const float p0 = (x[c] == -INFINITY) ? 0.f : exp2f(x[c] - m_new);
-        const float p1 = (x[c + 1] == -INFINITY) ? 0.f : exp2f(x[c + 1] - m_new);
-        rsum += p0 + p1;
-        pk[c >> 1] = pack_half2(p0, p1);
+          for (int u = 0; u < 32; ++u) pk[u] = 0u;
+        }
+        tmem_st32(lane_base + s_col, pk);
       }
-      l_run = l_run * alpha + rsum;
+      if (nblk == 2) {
+        uint32_t pk[32];
+        if (mem1) rs += exp_pack64(sr + 64, cl2, negm, pk);
+        else {
+#pragma unroll
+          for (int u = 0; u < 32; ++u) pk[u] = 0u;
+        }
+        tmem_st32(lane_base + s_col + 32, pk);
+      }
+      l_run = l_run * alpha + rs;
       m_run = m_new;
-
-      if (j > 0) {
-        // PV(j-1) done: O is stable and the P buffer is free.
+      if (__any_sync(0xffffffffu, rescale)) {
+        // PV(j-1) must be done before O is scaled (j > 0 here: m_run was finite).
         if (!mbar_wait_warp(bar(L::bOReady), (j - 1) & 1, abort_sig)) { ok = false; break; }
         tc_fence_after();
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
           uint32_t o[32];
+          tmem_ld32(lane_base + kColO + 32 * c, o);
+          tmem_wait_ld();
 #pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            tmem_ld32(lane_base + kColO + 32 * c, o);
-            tmem_wait_ld();
-#pragma unroll
-            for (int u = 0; u < 32; ++u) o[u] = __float_as_uint(__uint_as_float(o[u]) * alpha);
-            tmem_st32(lane_base + kColO + 32 * c, o);
-          }
-          tmem_wait_st();
+          for (int u = 0; u < 32; ++u) o[u] = __float_as_uint(__uint_as_float(o[u]) * alpha);
+          tmem_st32(lane_base + kColO + 32 * c, o);
         }
       }
-      // P row -> shared memory, K-major, 128-byte swizzle (chunk ^ row%8).
-      {
-        uint8_t* prow = smem + L::kP + r * 128;
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          if (c >= 8 && nblk == 1) break;
-          const int kh = c >> 3, ch = c & 7;
-          uint4 v = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-          *reinterpret_cast<uint4*>(prow + kh * L::kRegion + ((ch ^ (r & 7)) << 4)) = v;
-        }
-      }
-      fence_proxy_async_smem();
+      tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar(L::bPFull));
     }
@@ -400,7 +426,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     // ------------------------------------------------------------ epilogue
     bool have_o = ok && n_steps > 0;
     if (have_o) {
-      have_o = mbar_wait_warp(bar(L::bOReady), (n_steps - 1) & 1, abort_sig);
+      // The MMA thread commits bFin after its last PV; softmax need not have
+      // seen every o_ready phase, so that barrier's parity is no guide here.
+      have_o = mbar_wait_warp(bar(L::bFin), 0, abort_sig);
       if (!have_o) {
         *abort_flag = 1;
         set_status(a.dev_status, SA_DEV_TIMEOUT);
@@ -410,26 +438,24 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const bool row_ok = t < S;
     const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
     uint16_t* orow = a.o + b * a.os[0] + static_cast<int64_t>(t) * a.os[1] + h * a.os[2];
+    uint32_t o[D];
+    if (have_o) {
 #pragma unroll
-    for (int c = 0; c < D / 32; ++c) {
-      uint32_t o[32];
-      if (have_o) {
-        tmem_ld32(lane_base + kColO + 32 * c, o);
-        tmem_wait_ld();
-      } else {
+      for (int c = 0; c < D / 32; ++c) tmem_ld32(lane_base + kColO + 32 * c, o + 32 * c);
+      tmem_wait_ld();
+    } else {
 #pragma unroll
-        for (int u = 0; u < 32; ++u) o[u] = 0u;
-      }
-      if (row_ok) {
+      for (int u = 0; u < D; ++u) o[u] = 0u;
+    }
+    if (row_ok) {
 #pragma unroll
-        for (int v = 0; v < 4; ++v) {
-          uint4 w;
-          w.x = pack_bf162(__uint_as_float(o[8 * v + 0]) * inv_l, __uint_as_float(o[8 * v + 1]) * inv_l);
-          w.y = pack_bf162(__uint_as_float(o[8 * v + 2]) * inv_l, __uint_as_float(o[8 * v + 3]) * inv_l);
-          w.z = pack_bf162(__uint_as_float(o[8 * v + 4]) * inv_l, __uint_as_float(o[8 * v + 5]) * inv_l);
-          w.w = pack_bf162(__uint_as_float(o[8 * v + 6]) * inv_l, __uint_as_float(o[8 * v + 7]) * inv_l);
-          *reinterpret_cast<uint4*>(orow + 32 * c + 8 * v) = w;
-        }
+      for (int v = 0; v < D / 8; ++v) {
+        uint4 w;
+        w.x = pack_bf162(__uint_as_float(o[8 * v + 0]) * inv_l, __uint_as_float(o[8 * v + 1]) * inv_l);
+        w.y = pack_bf162(__uint_as_float(o[8 * v + 2]) * inv_l, __uint_as_float(o[8 * v + 3]) * inv_l);
+        w.z = pack_bf162(__uint_as_float(o[8 * v + 4]) * inv_l, __uint_as_float(o[8 * v + 5]) * inv_l);
+        w.w = pack_bf162(__uint_as_float(o[8 * v + 6]) * inv_l, __uint_as_float(o[8 * v + 7]) * inv_l);
+        *reinterpret_cast<uint4*>(orow + 8 * v) = w;
       }
     }
     if (row_ok && a.lse) {

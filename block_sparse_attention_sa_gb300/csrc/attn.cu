@@ -12,17 +12,21 @@
 // walks the ascending union of the two blocks' key lists, two 64-key blocks
 // per step (N = 128); a key block listed for only one of the two query
 // blocks is masked to -inf for the other half's rows, so each row still sees
-// exactly its own key set. Six warps:
-//   warps 0-3  softmax + epilogue, one thread per query row (TMEM lane)
-//   warp  4    builds the tile's key-block union in shared memory, then one
+// exactly its own key set. Ten warps:
+//   warps 0-7  softmax + epilogue: two threads per query row (TMEM lane);
+//              warps 0-3 take the step's first key block and the first half
+//              of O's columns, warps 4-7 (same lanes) the second; the pair
+//              swaps its row max through shared memory every step
+//   warp  8    builds the tile's key-block union in shared memory, then one
 //              lane issues every TMA load (Q once; K and V^T per step)
-//   warp  5    allocates TMEM; one lane issues every tcgen05.mma
-// Pipeline per step j: K(j) -> S[j%2] = Q K^T (bf16, fp32 in TMEM)
+//   warp  9    allocates TMEM; one lane issues every tcgen05.mma
+// Pipeline per step j: K(j) -> S[j%3] = Q K^T (bf16, fp32 in TMEM)
 //   -> softmax(j) reads S, writes P (fp16) back over the same TMEM columns,
 //   and rescales O in TMEM only when the running max moved by more than 2^8
-//   -> O += P V with P read from TMEM (fp16, fp32 accumulation). The tensor
-//   pipe runs QK^T(j+1) and PV(j) while softmax(j+1) runs; softmax waits for
-//   the previous PV only when it has to rescale O.
+//   -> O += P V with P read from TMEM (fp16, fp32 accumulation). With three
+//   S buffers the MMA thread issues PV(j) as soon as P(j) is ready and then
+//   QK(j+3), so QK(j+1) and QK(j+2) are already queued while softmax(j)
+//   runs; softmax waits for the previous PV only when it has to rescale O.
 // The producer alone reads the route, before the pipeline starts, so no
 // data-dependent load sits inside the pipelined loops.
 // Every wait is bounded (SA_DEV_TIMEOUT) and an aborted CTA drains its own
@@ -40,11 +44,14 @@ namespace {
 
 constexpr int BM = 128;   // query rows per tile
 constexpr int BN = 128;   // key rows per step (two key blocks)
-constexpr int KST = 3;    // K stages
-constexpr int VST = 2;    // V stages
-constexpr int kThreads = 192;
+constexpr int KST = 3;    // K stages (= S buffers: s_full[j%3] also frees K stage j%3)
+constexpr int VST = 2;    // V stages (= o_ready barriers: o_ready[j%2] frees V stage j%2)
+constexpr int kThreads = 320;
+constexpr int kSoftmaxThreads = 256;
+constexpr int kProducerWarp = 8, kMmaWarp = 9;
 constexpr int kTmemCols = 512;
-constexpr int kColS0 = 0, kColS1 = 128, kColO = 256;
+constexpr int kNumS = 3;                 // S/P buffers in TMEM (128 columns each)
+constexpr int kColO = kNumS * 128;       // O accumulator columns [384, 384 + D)
 constexpr float kRescaleLog2 = 8.0f;  // lazy-rescale threshold: P <= 2^8 in fp16
 
 template <int D>
@@ -61,16 +68,18 @@ struct Smem {
   // barriers
   static constexpr int bQFull = 0;
   static constexpr int bKFull = 1;
-  static constexpr int bKEmpty = bKFull + KST;
-  static constexpr int bVFull = bKEmpty + KST;
-  static constexpr int bVEmpty = bVFull + VST;
-  static constexpr int bSFull = bVEmpty + VST;
-  static constexpr int bPFull = bSFull + 2;
-  static constexpr int bOReady = bPFull + 1;
-  static constexpr int bFin = bOReady + 1;
+  static constexpr int bVFull = bKFull + KST;
+  // QK(j) done (s_full[j%3]) frees K stage j%3, and PV(j) done
+  // (o_ready[j%2]) frees V stage j%2, so the producers wait on those.
+  static constexpr int bSFull = bVFull + VST;      // one per S buffer
+  static constexpr int bPFull = bSFull + kNumS;     // one per S buffer (see below)
+  static constexpr int bOReady = bPFull + kNumS;    // two, alternating by step parity
+  static constexpr int bFin = bOReady + 2;
   static constexpr int kNumBars = bFin + 1;
   static constexpr int kMisc = kBar + kNumBars * 8;   // tmem base, abort, n_entries
-  static constexpr int kBits = kMisc + 64;
+  static constexpr int kRed = kMisc + 64;             // [2 parities][2 halves][128] row maxima
+  static constexpr int kLRed = kRed + 2 * 2 * BM * 4; // [2 halves][128] row sums
+  static constexpr int kBits = kLRed + 2 * BM * 4;
   static constexpr int kInfo = kBits + 2 * (kMaxNbAttn / 32) * 4;
   static constexpr int kEnd = kInfo + kMaxNbAttn * 2;
   static constexpr int kBytes = kEnd + 1024;          // slack to align the base to 1 KB
@@ -88,6 +97,16 @@ __device__ __forceinline__ uint32_t pack_bf162(float a, float b) {
 
 __device__ __forceinline__ void set_status(int32_t* st, int bits) {
   if (st) atomicOr(st, bits);
+}
+
+// Wait sites, recorded as bit (8 + site) next to SA_DEV_TIMEOUT when a wait
+// gives up, so a status word names the stage that stalled.
+enum WaitSite {
+  kSiteKEmpty = 0, kSiteVEmpty, kSiteQFull, kSiteKFull, kSitePFull, kSiteVFull,
+  kSiteSFull, kSiteOReady, kSiteFin
+};
+__device__ __forceinline__ void note_timeout(int32_t* st, int site) {
+  set_status(st, SA_DEV_TIMEOUT | (1 << (8 + site)));
 }
 
 // max over 64 fp32 values (bit patterns), eight independent chains.
@@ -153,16 +172,22 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   // ---------------------------------------------------------------- setup
   if (threadIdx.x == 0) {
     // p_full: every softmax thread arrives; the rest: one arrival (TMA
-    // expect_tx or tcgen05.commit).
-    for (int i = 0; i < L::kNumBars; ++i) mbar_init(bar(i), i == L::bPFull ? BM : 1);
+    // expect_tx or tcgen05.commit). There is one p_full per S buffer: the
+    // softmax may finish several steps before the MMA thread looks, but the
+    // next phase of p_full[j%3] needs QK(j+3), which the MMA thread issues
+    // only after it has seen phase j, so a parity wait never falls a full
+    // round behind. (The same holds for every other barrier here: none can
+    // complete its next phase before its waiter has seen the current one.)
+    for (int i = 0; i < L::kNumBars; ++i)
+      mbar_init(bar(i), (i >= L::bPFull && i < L::bPFull + kNumS) ? kSoftmaxThreads : 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tmem_alloc(sbase + L::kMisc, kTmemCols);
     tmem_relinquish();
   }
-  if (warp == 4) {
+  if (warp == kProducerWarp) {
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
@@ -223,54 +248,65 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   const int n_entries = static_cast<int>(misc[2]);
   const int n_steps = (n_entries + 1) >> 1;
 
-  if (warp == 4) {
+  if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
+    // Lane 0 streams Q and then K, lane 1 streams V, each as far ahead as its
+    // ring allows, so a K load never waits behind a V stage or vice versa.
+    // Each lane waits for all of its own copies to land before it leaves, so
+    // no copy can outlive the CTA's shared memory.
     if (lane == 0) {
-      int k_issued[KST] = {0}, v_issued[VST] = {0};
+      int issued[KST] = {0};
       bool ok = true;
       mbar_arrive_expect_tx(bar(L::bQFull), L::kQBytes);
       for (int qh = 0; qh < 2; ++qh)
         for (int dh = 0; dh < D / 64; ++dh)
           tma_load_4d(sbase + L::kQ + dh * L::kRegion + qh * 8192, &tm_q, bar(L::bQFull),
                       dh * 64, (qb0 + qh) * kBlock, h, b);
-      for (int j = 0; j < n_steps && ok; ++j) {
+      for (int j = 0; j < n_steps; ++j) {
         const int nblk = (2 * j + 1 < n_entries) ? 2 : 1;
         const int ks = j % KST;
-        if (j >= KST) ok = mbar_wait(bar(L::bKEmpty + ks), ((j / KST) - 1) & 1, abort_sig);
-        if (!ok) break;
+        if (j >= KST && !mbar_wait(bar(L::bSFull + ks), ((j / KST) - 1) & 1, abort_sig)) {
+          note_timeout(a.dev_status, kSiteKEmpty);
+          ok = false;
+          break;
+        }
         mbar_arrive_expect_tx(bar(L::bKFull + ks), nblk * kBlock * D * 2);
-        ++k_issued[ks];
+        ++issued[ks];
         for (int kh = 0; kh < nblk; ++kh) {
           const int jk = info[2 * j + kh] >> 2;
           for (int dh = 0; dh < D / 64; ++dh)
             tma_load_4d(sbase + L::kK + ks * L::kKBytes + dh * L::kRegion + kh * 8192, &tm_k,
                         bar(L::bKFull + ks), dh * 64, jk * kBlock, h, b);
         }
+      }
+      if (!ok) *abort_flag = 1;
+      mbar_wait(bar(L::bQFull), 0, drain_sig);
+      for (int s2 = 0; s2 < KST; ++s2)
+        if (issued[s2]) mbar_wait(bar(L::bKFull + s2), (issued[s2] - 1) & 1, drain_sig);
+    } else if (lane == 1) {
+      int issued[VST] = {0};
+      bool ok = true;
+      for (int j = 0; j < n_steps; ++j) {
+        const int nblk = (2 * j + 1 < n_entries) ? 2 : 1;
         const int vs = j % VST;
-        if (j >= VST) ok = mbar_wait(bar(L::bVEmpty + vs), ((j / VST) - 1) & 1, abort_sig);
-        if (!ok) break;
+        if (j >= VST && !mbar_wait(bar(L::bOReady + vs), ((j / VST) - 1) & 1, abort_sig)) {
+          note_timeout(a.dev_status, kSiteVEmpty);
+          ok = false;
+          break;
+        }
         mbar_arrive_expect_tx(bar(L::bVFull + vs), nblk * kBlock * D * 2);
-        ++v_issued[vs];
+        ++issued[vs];
         for (int kh = 0; kh < nblk; ++kh) {
           const int jk = info[2 * j + kh] >> 2;
           tma_load_3d(sbase + L::kV + vs * L::kVBytes + kh * L::kVHalf, &tm_vt,
                       bar(L::bVFull + vs), jk * kBlock, 0, b * a.H + h);
         }
       }
-      if (!ok) {
-        *abort_flag = 1;
-        set_status(a.dev_status, SA_DEV_TIMEOUT);
-      }
-      if (*abort_flag) {
-        // Drain: every copy this CTA started lands before shared memory goes away.
-        mbar_wait(bar(L::bQFull), 0, drain_sig);
-        for (int s = 0; s < KST; ++s)
-          if (k_issued[s]) mbar_wait(bar(L::bKFull + s), (k_issued[s] - 1) & 1, drain_sig);
-        for (int s = 0; s < VST; ++s)
-          if (v_issued[s]) mbar_wait(bar(L::bVFull + s), (v_issued[s] - 1) & 1, drain_sig);
-      }
+      if (!ok) *abort_flag = 1;
+      for (int s2 = 0; s2 < VST; ++s2)
+        if (issued[s2]) mbar_wait(bar(L::bVFull + s2), (issued[s2] - 1) & 1, drain_sig);
     }
-  } else if (warp == 5) {
+  } else if (warp == kMmaWarp) {
     // ----------------------------------------------------------------- MMA
     if (lane == 0) {
       constexpr uint32_t kIdQK128 = idesc_f16(BM, 128, 1);
@@ -278,44 +314,66 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       constexpr uint32_t kIdPV = idesc_f16(BM, D, 0);
       // Q always lands before the CTA can exit, even with an empty route.
       bool ok = mbar_wait(bar(L::bQFull), 0, abort_sig);
+      if (!ok) note_timeout(a.dev_status, kSiteQFull);
+      // Descriptors: fixed high words, start addresses stepped in the low word.
+      const uint64_t q_desc = sdesc_kmajor_sw128(sbase + L::kQ);
+      const uint64_t k_desc = sdesc_kmajor_sw128(sbase + L::kK);
+      const uint64_t v_desc = sdesc_kmajor_sw128(sbase + L::kV);
+      const uint32_t desc_hi = static_cast<uint32_t>(q_desc >> 32);
+      const uint32_t q_lo = static_cast<uint32_t>(q_desc);
+      const uint32_t k_lo = static_cast<uint32_t>(k_desc);
+      const uint32_t v_lo = static_cast<uint32_t>(v_desc);
       auto issue_qk = [&](int j) -> bool {
         const int ks = j % KST;
-        if (!mbar_wait(bar(L::bKFull + ks), (j / KST) & 1, abort_sig)) return false;
+        if (!mbar_wait(bar(L::bKFull + ks), (j / KST) & 1, abort_sig)) {
+          note_timeout(a.dev_status, kSiteKFull);
+          return false;
+        }
         tc_fence_after();
-        const int nblk = (2 * j + 1 < n_entries) ? 2 : 1;
-        const uint32_t d_tmem = tmem + ((j & 1) ? kColS1 : kColS0);
-        const uint32_t qa = sbase + L::kQ, kb = sbase + L::kK + ks * L::kKBytes;
+        const uint32_t idesc = (2 * j + 1 < n_entries) ? kIdQK128 : kIdQK64;
+        const uint32_t d_tmem = tmem + (j % kNumS) * 128;
+        const uint32_t kb = k_lo + ks * (L::kKBytes >> 4);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * L::kRegion + (kk & 3) * 32;
-          umma_ss(d_tmem, sdesc_kmajor_sw128(qa + off), sdesc_kmajor_sw128(kb + off),
-                  nblk == 2 ? kIdQK128 : kIdQK64, kk > 0);
+          const uint32_t off = ((kk >> 2) * L::kRegion + (kk & 3) * 32) >> 4;
+          umma_ss_lohi(d_tmem, q_lo + off, desc_hi, kb + off, desc_hi, idesc, kk > 0);
         }
-        umma_commit(bar(L::bSFull + (j & 1)));
-        umma_commit(bar(L::bKEmpty + ks));
+        umma_commit(bar(L::bSFull + (j % kNumS)));
         return true;
       };
-      if (ok && n_steps > 0) {
-        tc_fence_after();
-        ok = issue_qk(0);
-      }
+      if (ok && n_steps > 0) tc_fence_after();
+      for (int j = 0; j < kNumS && j < n_steps && ok; ++j) ok = issue_qk(j);
       for (int j = 0; j < n_steps && ok; ++j) {
-        if (j + 1 < n_steps && !issue_qk(j + 1)) { ok = false; break; }
-        if (!mbar_wait(bar(L::bPFull), j & 1, abort_sig)) { ok = false; break; }
+        if (!mbar_wait(bar(L::bPFull + j % kNumS), (j / kNumS) & 1, abort_sig)) {
+          note_timeout(a.dev_status, kSitePFull);
+          ok = false;
+          break;
+        }
         tc_fence_after();
         const int vs = j % VST;
-        if (!mbar_wait(bar(L::bVFull + vs), (j / VST) & 1, abort_sig)) { ok = false; break; }
-        tc_fence_after();
-        const int nblk = (2 * j + 1 < n_entries) ? 2 : 1;
-        const uint32_t pa = tmem + ((j & 1) ? kColS1 : kColS0);  // P(j) over S(j)
-        const uint32_t vb = sbase + L::kV + vs * L::kVBytes;
-        for (int kk = 0; kk < nblk * 4; ++kk) {
-          const uint32_t kh = kk >> 2, off = (kk & 3) * 32;
-          umma_ts(tmem + kColO, pa + 8 * kk, sdesc_kmajor_sw128(vb + kh * L::kVHalf + off), kIdPV,
-                  (j > 0 || kk > 0));
+        if (!mbar_wait(bar(L::bVFull + vs), (j / VST) & 1, abort_sig)) {
+          note_timeout(a.dev_status, kSiteVFull);
+          ok = false;
+          break;
         }
-        umma_commit(bar(L::bOReady));
-        umma_commit(bar(L::bVEmpty + vs));
+        tc_fence_after();
+        const uint32_t pa = tmem + (j % kNumS) * 128;  // P(j) over S(j)
+        const uint32_t vb = v_lo + vs * (L::kVBytes >> 4);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          umma_ts_lohi(tmem + kColO, pa + 8 * kk, vb + ((kk & 3) * 32 >> 4), desc_hi, kIdPV,
+                       (j > 0 || kk > 0));
+        if (2 * j + 1 < n_entries) {
+#pragma unroll
+          for (int kk = 4; kk < 8; ++kk)
+            umma_ts_lohi(tmem + kColO, pa + 8 * kk,
+                         vb + ((L::kVHalf + (kk & 3) * 32) >> 4), desc_hi, kIdPV, 1u);
+        }
+        umma_commit(bar(L::bOReady + (j & 1)));
+        // S[j%3] now belongs to QK(j+3): PV(j), the last reader of P(j), was
+        // issued just before, and the tensor pipe runs this thread's MMAs in
+        // order.
+        if (j + kNumS < n_steps && !issue_qk(j + kNumS)) { ok = false; break; }
       }
       if (!ok) {
         *abort_flag = 1;
@@ -327,96 +385,103 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
   } else {
     // ------------------------------------------------------------- softmax
-    const int r = threadIdx.x;                 // tile row == TMEM lane
+    // Two threads per row: `half` 0 owns the step's first key block and O
+    // columns [0, D/2); `half` 1 the second block and O columns [D/2, D).
+    // The pair meets at named barrier 1 + quarter every step, so a thread
+    // that gives up on a wait keeps looping (skipping all waits and TMEM
+    // work) to keep the pair's barrier counts equal.
+    const int quarter = warp & 3, half = warp >> 2;
+    const int r = quarter * 32 + lane;         // tile row == TMEM lane
     const int qh = r >> 6;                     // query block of this row (warp-uniform)
     const int t = qb0 * kBlock + r;            // query token
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const int last_valid = S - (Nb - 1) * kBlock;  // tokens in the last block
     const float cl2 = a.scale_log2;
+    float* red = reinterpret_cast<float*>(smem + L::kRed);
+    float* lred = reinterpret_cast<float*>(smem + L::kLRed);
+    const uint32_t pair_bar = 1 + quarter;
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
 
     for (int j = 0; j < n_steps; ++j) {
-      if (!mbar_wait_warp(bar(L::bSFull + (j & 1)), (j >> 1) & 1, abort_sig)) { ok = false; break; }
-      tc_fence_after();
+      if (ok && !mbar_wait_warp(bar(L::bSFull + j % kNumS), (j / kNumS) & 1, abort_sig)) {
+        ok = false;
+        if (lane == 0) note_timeout(a.dev_status, kSiteSFull);
+      }
+      if (ok) tc_fence_after();
       const int nblk = (2 * j + 1 < n_entries) ? 2 : 1;
-      const uint32_t e0 = info[2 * j];
-      const uint32_t e1 = nblk == 2 ? info[2 * j + 1] : 0u;
-      const bool mem0 = (e0 >> qh) & 1u;
-      const bool mem1 = nblk == 2 && ((e1 >> qh) & 1u);
-      const uint32_t s_col = (j & 1) ? kColS1 : kColS0;
+      const bool present = half == 0 || nblk == 2;
+      const uint32_t e = present ? info[2 * j + half] : 0u;
+      const bool mem = ok && present && ((e >> qh) & 1u);
+      const uint32_t s_col = (j % kNumS) * 128;
 
-      uint32_t sr[BN];
-      if (mem0) {
-        tmem_ld32(lane_base + s_col, sr);
-        tmem_ld32(lane_base + s_col + 32, sr + 32);
-      }
-      if (mem1) {
-        tmem_ld32(lane_base + s_col + 64, sr + 64);
-        tmem_ld32(lane_base + s_col + 96, sr + 96);
-      }
-      tmem_wait_ld();
-      // the ragged last block: keys past S weigh exactly zero
-      if (mem0 && static_cast<int>(e0 >> 2) == Nb - 1) {
+      uint32_t sr[64];
+      float my_max = -INFINITY;
+      if (mem) {
+        tmem_ld32(lane_base + s_col + 64 * half, sr);
+        tmem_ld32(lane_base + s_col + 64 * half + 32, sr + 32);
+        tmem_wait_ld();
+        if (static_cast<int>(e >> 2) == Nb - 1) {  // ragged last block: keys past S weigh 0
 #pragma unroll
-        for (int u = 0; u < 64; ++u)
-          if (u >= last_valid) sr[u] = __float_as_uint(-INFINITY);
+          for (int u = 0; u < 64; ++u)
+            if (u >= last_valid) sr[u] = __float_as_uint(-INFINITY);
+        }
+        my_max = max64(sr);
       }
-      if (mem1 && static_cast<int>(e1 >> 2) == Nb - 1) {
-#pragma unroll
-        for (int u = 0; u < 64; ++u)
-          if (u >= last_valid) sr[64 + u] = __float_as_uint(-INFINITY);
-      }
-      float mx = -INFINITY;
-      if (mem0) mx = fmaxf(mx, max64(sr));
-      if (mem1) mx = fmaxf(mx, max64(sr + 64));
+      float* slot = red + (j & 1) * 2 * BM;
+      slot[half * BM + r] = my_max;
+      // the partner's S loads are ordered before this thread's P stores,
+      // which overwrite S columns 32-63 of the partner's half
+      tc_fence_before();
+      named_bar_sync(pair_bar, 64);
+      tc_fence_after();
+      const float mx = fmaxf(my_max, slot[(half ^ 1) * BM + r]);
+      if (!ok) continue;
       const float bmax = mx * cl2;           // the scale is positive: max commutes
       float m_new = m_run;
       if (bmax > m_run + kRescaleLog2) m_new = bmax;  // also the first finite block
       const bool rescale = (m_new != m_run) && (m_run != -INFINITY);
       const float alpha = (m_new == m_run) ? 1.f : fast_exp2(m_run - m_new);
-      const float negm = -m_new;
       // P(j) over the consumed S(j) columns: keys 0-63 -> columns 0-31,
-      // keys 64-127 -> columns 32-63 (two fp16 per column). Each half is
-      // stored as soon as it is ready, so only 32 packed words stay live.
+      // keys 64-127 -> columns 32-63 (two fp16 per column).
       float rs = 0.f;
-      {
+      if (present) {
         uint32_t pk[32];
-        if (mem0) rs += exp_pack64(sr, cl2, negm, pk);
+        if (mem) rs = exp_pack64(sr, cl2, -m_new, pk);
         else {
 #pragma unroll
           for (int u = 0; u < 32; ++u) pk[u] = 0u;
         }
-        tmem_st32(lane_base + s_col, pk);
-      }
-      if (nblk == 2) {
-        uint32_t pk[32];
-        if (mem1) rs += exp_pack64(sr + 64, cl2, negm, pk);
-        else {
-#pragma unroll
-          for (int u = 0; u < 32; ++u) pk[u] = 0u;
-        }
-        tmem_st32(lane_base + s_col + 32, pk);
+        tmem_st32(lane_base + s_col + 32 * half, pk);
       }
       l_run = l_run * alpha + rs;
       m_run = m_new;
       if (__any_sync(0xffffffffu, rescale)) {
-        // PV(j-1) must be done before O is scaled (j > 0 here: m_run was finite).
-        if (!mbar_wait_warp(bar(L::bOReady), (j - 1) & 1, abort_sig)) { ok = false; break; }
+        // PV(j-1) must be done before O is scaled (j > 0 here: m_run was
+        // finite). S(j) ready implies PV(j-3) done (QK(j) was issued after
+        // it) and PV(j+1) is not yet issued, so on the barrier of PV(j-1)'s
+        // parity the phase of PV(j-1) is either the last completed or the
+        // pending one: no ambiguity.
+        if (!mbar_wait_warp(bar(L::bOReady + ((j - 1) & 1)), ((j - 1) >> 1) & 1, abort_sig)) {
+          ok = false;
+          if (lane == 0) note_timeout(a.dev_status, kSiteOReady);
+          continue;
+        }
         tc_fence_after();
 #pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
+        for (int c = 0; c < D / 64; ++c) {
           uint32_t o[32];
-          tmem_ld32(lane_base + kColO + 32 * c, o);
+          const uint32_t col = kColO + half * (D / 2) + 32 * c;
+          tmem_ld32(lane_base + col, o);
           tmem_wait_ld();
 #pragma unroll
           for (int u = 0; u < 32; ++u) o[u] = __float_as_uint(__uint_as_float(o[u]) * alpha);
-          tmem_st32(lane_base + kColO + 32 * c, o);
+          tmem_st32(lane_base + col, o);
         }
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(bar(L::bPFull));
+      mbar_arrive(bar(L::bPFull + j % kNumS));
     }
     if (!ok) {
       *abort_flag = 1;
@@ -424,6 +489,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
 
     // ------------------------------------------------------------ epilogue
+    lred[half * BM + r] = l_run;
+    named_bar_sync(pair_bar, 64);
+    const float l_tot = l_run + lred[(half ^ 1) * BM + r];
     bool have_o = ok && n_steps > 0;
     if (have_o) {
       // The MMA thread commits bFin after its last PV; softmax need not have
@@ -431,25 +499,27 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       have_o = mbar_wait_warp(bar(L::bFin), 0, abort_sig);
       if (!have_o) {
         *abort_flag = 1;
-        set_status(a.dev_status, SA_DEV_TIMEOUT);
+        if (lane == 0) note_timeout(a.dev_status, kSiteFin);
       }
       tc_fence_after();
     }
     const bool row_ok = t < S;
-    const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
-    uint16_t* orow = a.o + b * a.os[0] + static_cast<int64_t>(t) * a.os[1] + h * a.os[2];
-    uint32_t o[D];
+    const float inv_l = l_tot > 0.f ? 1.f / l_tot : 0.f;
+    uint16_t* orow = a.o + b * a.os[0] + static_cast<int64_t>(t) * a.os[1] + h * a.os[2] +
+                     half * (D / 2);
+    uint32_t o[D / 2];
     if (have_o) {
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) tmem_ld32(lane_base + kColO + 32 * c, o + 32 * c);
+      for (int c = 0; c < D / 64; ++c)
+        tmem_ld32(lane_base + kColO + half * (D / 2) + 32 * c, o + 32 * c);
       tmem_wait_ld();
     } else {
 #pragma unroll
-      for (int u = 0; u < D; ++u) o[u] = 0u;
+      for (int u = 0; u < D / 2; ++u) o[u] = 0u;
     }
     if (row_ok) {
 #pragma unroll
-      for (int v = 0; v < D / 8; ++v) {
+      for (int v = 0; v < D / 16; ++v) {
         uint4 w;
         w.x = pack_bf162(__uint_as_float(o[8 * v + 0]) * inv_l, __uint_as_float(o[8 * v + 1]) * inv_l);
         w.y = pack_bf162(__uint_as_float(o[8 * v + 2]) * inv_l, __uint_as_float(o[8 * v + 3]) * inv_l);
@@ -458,8 +528,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         *reinterpret_cast<uint4*>(orow + 8 * v) = w;
       }
     }
-    if (row_ok && a.lse) {
-      const float lse = l_run > 0.f ? m_run * 0.69314718055994531f + logf(l_run) : -INFINITY;
+    if (row_ok && half == 0 && a.lse) {
+      const float lse = l_tot > 0.f ? m_run * 0.69314718055994531f + logf(l_tot) : -INFINITY;
       a.lse[(static_cast<int64_t>(b) * a.H + h) * S + t] = lse;
     }
   }
@@ -467,7 +537,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 5) tmem_dealloc(tmem, kTmemCols);
+  if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
 }
 
 // V [B,S,H,D] bf16 -> vt [B*H][D][s_pad] fp16. grid (ceil(S/64), H, B), 256 threads.

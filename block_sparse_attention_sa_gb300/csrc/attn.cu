@@ -7,30 +7,30 @@
 // execution", third paragraph: the exact prefix sink and the diagonal are
 // part of every route). Dense mode lists every key block.
 //
-// Tile and roles. One CTA owns a 128-row query tile = query blocks 2p and
-// 2p+1 of one head (tcgen05 M = 128; the route is per 64-row block). It
-// walks the ascending union of the two blocks' key lists, two 64-key blocks
-// per step (N = 128); a key block listed for only one of the two query
-// blocks is masked to -inf for the other half's rows, so each row still sees
-// exactly its own key set. Ten warps:
-//   warps 0-7  softmax + epilogue: two threads per query row (TMEM lane);
-//              warps 0-3 take the step's first key block and the first half
-//              of O's columns, warps 4-7 (same lanes) the second; the pair
-//              swaps its row max through shared memory every step
-//   warp  8    builds the tile's key-block union in shared memory, then one
-//              lane issues every TMA load (Q once; K and V^T per step)
-//   warp  9    allocates TMEM; one lane issues every tcgen05.mma
-// Pipeline per step j: K(j) -> S[j%3] = Q K^T (bf16, fp32 in TMEM)
-//   -> softmax(j) reads S, writes P (fp16) back over the same TMEM columns,
-//   and rescales O in TMEM only when the running max moved by more than 2^8
-//   -> O += P V with P read from TMEM (fp16, fp32 accumulation). With three
-//   S buffers the MMA thread issues PV(j) as soon as P(j) is ready and then
-//   QK(j+3), so QK(j+1) and QK(j+2) are already queued while softmax(j)
-//   runs; softmax waits for the previous PV only when it has to rescale O.
-// The producer alone reads the route, before the pipeline starts, so no
-// data-dependent load sits inside the pipelined loops.
-// Every wait is bounded (SA_DEV_TIMEOUT) and an aborted CTA drains its own
-// copies and MMAs and frees TMEM before it exits.
+// Tile. One CTA owns a 128-row query tile = query blocks 2p and 2p+1 of one
+// head (tcgen05 M = 128; the route is per 64-row block). It walks the union
+// of the two blocks' key lists, two 64-key blocks per step (N = 128); a key
+// block listed for only one of the two query blocks is masked to -inf for
+// the other half's rows, so each row still sees exactly its own key set.
+//
+// Split-K ping-pong. The walk's steps alternate between two softmax
+// warpgroups: group 0 takes the even steps, group 1 the odd ones. Each group
+// has its own S buffer, running max and sum, and O accumulator in TMEM
+// (S0 S1 O0 O1 = 4 x 128 columns), so one group's softmax runs while the
+// tensor pipe works on the other group's QK^T and PV, and each group gets
+// two steps of MMA time for its softmax. The two partial results are merged
+// once at the end (rescaled to the common max, summed, divided by the
+// common sum).
+//
+// Warps: 0-3 softmax group 0, 4-7 softmax group 1 (one thread per row =
+// TMEM lane), 8 route merge then TMA (lane 0: Q and K, lane 1: V), 9 TMEM
+// allocation then one lane issues every tcgen05.mma.
+// Step j: K(j) -> S[j%2] = Q K^T (bf16 x bf16 -> fp32) -> softmax(j) reads
+// S, writes P (fp16) over the same columns -> O[j%2] += P V (fp16, A from
+// TMEM) -> QK^T(j+2) reuses S[j%2]. The producer alone reads the route,
+// before the pipeline starts, so no data-dependent load sits inside the
+// pipelined loops. Every wait is bounded (SA_DEV_TIMEOUT) and an aborted CTA
+// drains its own copies and MMAs and frees TMEM before it exits.
 #include <cmath>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -44,15 +44,20 @@ namespace {
 
 constexpr int BM = 128;   // query rows per tile
 constexpr int BN = 128;   // key rows per step (two key blocks)
-constexpr int KST = 3;    // K stages (= S buffers: s_full[j%3] also frees K stage j%3)
-constexpr int VST = 2;    // V stages (= o_ready barriers: o_ready[j%2] frees V stage j%2)
+// Two K and two V stages: QK(j) done (s_full[j%2]) frees K stage j%2 and
+// PV(j) done (o_ready[j%2]) frees V stage j%2, so the producers wait on those.
+constexpr int KST = 2;
+constexpr int VST = 2;
 constexpr int kThreads = 320;
-constexpr int kSoftmaxThreads = 256;
+constexpr int kGroupThreads = 128;
 constexpr int kProducerWarp = 8, kMmaWarp = 9;
 constexpr int kTmemCols = 512;
-constexpr int kNumS = 3;                 // S/P buffers in TMEM (128 columns each)
-constexpr int kColO = kNumS * 128;       // O accumulator columns [384, 384 + D)
-constexpr float kRescaleLog2 = 8.0f;  // lazy-rescale threshold: P <= 2^8 in fp16
+constexpr int kColS = 0;      // S[g] at columns [128 g, 128 g + 128)
+constexpr int kColO = 256;    // O[g] at columns [256 + 128 g, 256 + 128 g + D)
+// Lazy rescale: the running max moves only when a block max exceeds it by
+// more than 2^14, so P <= 16384 stays well inside fp16; values that fall
+// below fp16's normal range weigh under 2^-28 of the row max.
+constexpr float kRescaleLog2 = 14.0f;
 
 template <int D>
 struct Smem {
@@ -65,21 +70,17 @@ struct Smem {
   static constexpr int kVBytes = BN * D * 2;
   static constexpr int kVHalf = D * 128;              // one 64-key half of a V^T stage
   static constexpr int kBar = kV + VST * kVBytes;
-  // barriers
   static constexpr int bQFull = 0;
-  static constexpr int bKFull = 1;
-  static constexpr int bVFull = bKFull + KST;
-  // QK(j) done (s_full[j%3]) frees K stage j%3, and PV(j) done
-  // (o_ready[j%2]) frees V stage j%2, so the producers wait on those.
-  static constexpr int bSFull = bVFull + VST;      // one per S buffer
-  static constexpr int bPFull = bSFull + kNumS;     // one per S buffer (see below)
-  static constexpr int bOReady = bPFull + kNumS;    // two, alternating by step parity
-  static constexpr int bFin = bOReady + 2;
+  static constexpr int bKFull = 1;                    // [KST]
+  static constexpr int bVFull = bKFull + KST;         // [VST]
+  static constexpr int bSFull = bVFull + VST;         // [2] QK(j) done, one per group
+  static constexpr int bPFull = bSFull + 2;           // [2] softmax(j) done, one per group
+  static constexpr int bOReady = bPFull + 2;          // [2] PV(j) done, one per group
+  static constexpr int bFin = bOReady + 2;            // every MMA done
   static constexpr int kNumBars = bFin + 1;
   static constexpr int kMisc = kBar + kNumBars * 8;   // tmem base, abort, n_entries
-  static constexpr int kRed = kMisc + 64;             // [2 parities][2 halves][128] row maxima
-  static constexpr int kLRed = kRed + 2 * 2 * BM * 4; // [2 halves][128] row sums
-  static constexpr int kBits = kLRed + 2 * BM * 4;
+  static constexpr int kXch = kMisc + 64;             // [2 groups][2 (m, l)][128] merge
+  static constexpr int kBits = kXch + 2 * 2 * BM * 4;
   static constexpr int kInfo = kBits + 2 * (kMaxNbAttn / 32) * 4;
   static constexpr int kEnd = kInfo + kMaxNbAttn * 2;
   static constexpr int kBytes = kEnd + 1024;          // slack to align the base to 1 KB
@@ -102,8 +103,8 @@ __device__ __forceinline__ void set_status(int32_t* st, int bits) {
 // Wait sites, recorded as bit (8 + site) next to SA_DEV_TIMEOUT when a wait
 // gives up, so a status word names the stage that stalled.
 enum WaitSite {
-  kSiteKEmpty = 0, kSiteVEmpty, kSiteQFull, kSiteKFull, kSitePFull, kSiteVFull,
-  kSiteSFull, kSiteOReady, kSiteFin
+  kSiteKStage = 0, kSiteVStage, kSiteQFull, kSiteKFull, kSitePFull, kSiteVFull,
+  kSiteSFull, kSiteFin
 };
 __device__ __forceinline__ void note_timeout(int32_t* st, int site) {
   set_status(st, SA_DEV_TIMEOUT | (1 << (8 + site)));
@@ -171,15 +172,15 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
   // ---------------------------------------------------------------- setup
   if (threadIdx.x == 0) {
-    // p_full: every softmax thread arrives; the rest: one arrival (TMA
-    // expect_tx or tcgen05.commit). There is one p_full per S buffer: the
-    // softmax may finish several steps before the MMA thread looks, but the
-    // next phase of p_full[j%3] needs QK(j+3), which the MMA thread issues
-    // only after it has seen phase j, so a parity wait never falls a full
-    // round behind. (The same holds for every other barrier here: none can
-    // complete its next phase before its waiter has seen the current one.)
+    // p_full[g]: the 128 threads of softmax group g arrive; every other
+    // barrier takes one arrival (TMA expect_tx or tcgen05.commit). No barrier
+    // can complete its next phase before its waiter has seen the current
+    // one: s_full[g]'s next phase needs QK(j+2), issued after p_full(j);
+    // p_full[g]'s needs S(j+2); k_full/v_full's need the stage freed after
+    // their consumer waited; o_ready[g]'s needs PV(j+2), which needs V(j+2),
+    // loaded only after the producer saw PV(j).
     for (int i = 0; i < L::kNumBars; ++i)
-      mbar_init(bar(i), (i >= L::bPFull && i < L::bPFull + kNumS) ? kSoftmaxThreads : 1);
+      mbar_init(bar(i), (i == L::bPFull || i == L::bPFull + 1) ? kGroupThreads : 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -193,13 +194,17 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_vt);
     }
-    // Union of the two query blocks' key lists, ascending, with a 2-bit
-    // membership mask per key block: bit 0 = block 2p lists it, bit 1 = 2p+1.
+    // Union of the two query blocks' key lists with a 2-bit membership mask
+    // per key block (bit 0: block 2p lists it, bit 1: block 2p+1 does),
+    // ascending but rotated to start at the tile's own diagonal block: the
+    // row maxima usually sit near the diagonal, so taking it first keeps
+    // later steps from raising the running max (each raise rescales O).
     const int words = (Nb + 31) >> 5;
     int bad = 0;
     if (a.row_ptr == nullptr) {
       const uint16_t m = has_qb1 ? 3 : 1;
-      for (int j = lane; j < Nb; j += 32) info[j] = static_cast<uint16_t>((j << 2) | m);
+      for (int j = lane; j < Nb; j += 32)
+        info[(j - qb0 + Nb) % Nb] = static_cast<uint16_t>((j << 2) | m);
       if (lane == 0) misc[2] = static_cast<uint32_t>(Nb);
     } else {
       for (int w = lane; w < words; w += 32) { bmA[w] = 0u; bmB[w] = 0u; }
@@ -217,7 +222,21 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
       }
       __syncwarp();
-      int total = 0;
+      // count the union and the entries below the diagonal (the rotation)
+      int total = 0, below = 0;
+      for (int w = lane; w < words; w += 32) {
+        const uint32_t u = bmA[w] | bmB[w];
+        total += __popc(u);
+        const int lo = w * 32;
+        const uint32_t below_mask =
+            qb0 >= lo + 32 ? 0xffffffffu : (qb0 <= lo ? 0u : ((1u << (qb0 - lo)) - 1u));
+        below += __popc(u & below_mask);
+      }
+      for (int off = 16; off >= 1; off >>= 1) {
+        total += __shfl_xor_sync(0xffffffffu, total, off);
+        below += __shfl_xor_sync(0xffffffffu, below, off);
+      }
+      int base = 0;
       for (int w0 = 0; w0 < words; w0 += 32) {
         const int w = w0 + lane;
         const uint32_t ua = w < words ? bmA[w] : 0u, ub = w < words ? bmB[w] : 0u;
@@ -228,14 +247,17 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           const int v = __shfl_up_sync(0xffffffffu, incl, off);
           if (lane >= off) incl += v;
         }
-        int pos = total + incl - c;
+        int pos = base + incl - c;
         while (u) {
           const int bit = __ffs(u) - 1;
           const uint32_t m = ((ua >> bit) & 1u) | (((ub >> bit) & 1u) << 1);
-          info[pos++] = static_cast<uint16_t>(((w * 32 + bit) << 2) | m);
+          int rp = pos - below;
+          if (rp < 0) rp += total;
+          info[rp] = static_cast<uint16_t>(((w * 32 + bit) << 2) | m);
+          ++pos;
           u &= u - 1;
         }
-        total += __shfl_sync(0xffffffffu, incl, 31);
+        base += __shfl_sync(0xffffffffu, incl, 31);
       }
       if (lane == 0) misc[2] = static_cast<uint32_t>(total);
     }
@@ -266,7 +288,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const int nblk = (2 * j + 1 < n_entries) ? 2 : 1;
         const int ks = j % KST;
         if (j >= KST && !mbar_wait(bar(L::bSFull + ks), ((j / KST) - 1) & 1, abort_sig)) {
-          note_timeout(a.dev_status, kSiteKEmpty);
+          note_timeout(a.dev_status, kSiteKStage);
           ok = false;
           break;
         }
@@ -290,7 +312,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const int nblk = (2 * j + 1 < n_entries) ? 2 : 1;
         const int vs = j % VST;
         if (j >= VST && !mbar_wait(bar(L::bOReady + vs), ((j / VST) - 1) & 1, abort_sig)) {
-          note_timeout(a.dev_status, kSiteVEmpty);
+          note_timeout(a.dev_status, kSiteVStage);
           ok = false;
           break;
         }
@@ -308,180 +330,182 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
   } else if (warp == kMmaWarp) {
     // ----------------------------------------------------------------- MMA
-    if (lane == 0) {
+    // The whole warp runs this loop in step (warp-uniform waits); elect.sync
+    // picks the lane that issues each batch of MMAs and each commit.
+    {
       constexpr uint32_t kIdQK128 = idesc_f16(BM, 128, 1);
       constexpr uint32_t kIdQK64 = idesc_f16(BM, 64, 1);
       constexpr uint32_t kIdPV = idesc_f16(BM, D, 0);
       // Q always lands before the CTA can exit, even with an empty route.
-      bool ok = mbar_wait(bar(L::bQFull), 0, abort_sig);
-      if (!ok) note_timeout(a.dev_status, kSiteQFull);
-      // Descriptors: fixed high words, start addresses stepped in the low word.
-      const uint64_t q_desc = sdesc_kmajor_sw128(sbase + L::kQ);
-      const uint64_t k_desc = sdesc_kmajor_sw128(sbase + L::kK);
-      const uint64_t v_desc = sdesc_kmajor_sw128(sbase + L::kV);
-      const uint32_t desc_hi = static_cast<uint32_t>(q_desc >> 32);
-      const uint32_t q_lo = static_cast<uint32_t>(q_desc);
-      const uint32_t k_lo = static_cast<uint32_t>(k_desc);
-      const uint32_t v_lo = static_cast<uint32_t>(v_desc);
+      bool ok = mbar_wait_warp(bar(L::bQFull), 0, abort_sig);
+      if (!ok && lane == 0) note_timeout(a.dev_status, kSiteQFull);
+      // Descriptors, built once: Q's K slices, and the K/V stage bases
+      // (start address stepped by 32 bytes inside a 128-byte swizzle row,
+      // then by one 16 KB region per 64 elements).
+      uint64_t qd[D / 16];
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk)
+        qd[kk] = sdesc_kmajor_sw128(sbase + L::kQ + (kk >> 2) * L::kRegion + (kk & 3) * 32);
+      const uint64_t k0 = sdesc_kmajor_sw128(sbase + L::kK);
+      const uint64_t v0 = sdesc_kmajor_sw128(sbase + L::kV);
       auto issue_qk = [&](int j) -> bool {
         const int ks = j % KST;
-        if (!mbar_wait(bar(L::bKFull + ks), (j / KST) & 1, abort_sig)) {
-          note_timeout(a.dev_status, kSiteKFull);
+        if (!mbar_wait_warp(bar(L::bKFull + ks), (j / KST) & 1, abort_sig)) {
+          if (lane == 0) note_timeout(a.dev_status, kSiteKFull);
           return false;
         }
         tc_fence_after();
         const uint32_t idesc = (2 * j + 1 < n_entries) ? kIdQK128 : kIdQK64;
-        const uint32_t d_tmem = tmem + (j % kNumS) * 128;
-        const uint32_t kb = k_lo + ks * (L::kKBytes >> 4);
+        const uint32_t d_tmem = tmem + kColS + (j & 1) * 128;
+        const uint64_t kb = k0 + static_cast<uint64_t>(ks * (L::kKBytes >> 4));
+        uint64_t kd[D / 16];
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = ((kk >> 2) * L::kRegion + (kk & 3) * 32) >> 4;
-          umma_ss_lohi(d_tmem, q_lo + off, desc_hi, kb + off, desc_hi, idesc, kk > 0);
-        }
-        umma_commit(bar(L::bSFull + (j % kNumS)));
+        for (int kk = 0; kk < D / 16; ++kk)
+          kd[kk] = kb + static_cast<uint64_t>(((kk >> 2) * L::kRegion + (kk & 3) * 32) >> 4);
+#pragma unroll
+        for (int g = 0; g < D / 64; ++g)
+          umma_ss_x4_elect(d_tmem, qd[4 * g], qd[4 * g + 1], qd[4 * g + 2], qd[4 * g + 3],
+                           kd[4 * g], kd[4 * g + 1], kd[4 * g + 2], kd[4 * g + 3], idesc, g > 0);
+        umma_commit_elect(bar(L::bSFull + (j & 1)));
         return true;
       };
       if (ok && n_steps > 0) tc_fence_after();
-      for (int j = 0; j < kNumS && j < n_steps && ok; ++j) ok = issue_qk(j);
+      for (int j = 0; j < 2 && j < n_steps && ok; ++j) ok = issue_qk(j);
       for (int j = 0; j < n_steps && ok; ++j) {
-        if (!mbar_wait(bar(L::bPFull + j % kNumS), (j / kNumS) & 1, abort_sig)) {
-          note_timeout(a.dev_status, kSitePFull);
+        const int g = j & 1;
+        if (!mbar_wait_warp(bar(L::bPFull + g), (j >> 1) & 1, abort_sig)) {
+          if (lane == 0) note_timeout(a.dev_status, kSitePFull);
           ok = false;
           break;
         }
         tc_fence_after();
         const int vs = j % VST;
-        if (!mbar_wait(bar(L::bVFull + vs), (j / VST) & 1, abort_sig)) {
-          note_timeout(a.dev_status, kSiteVFull);
+        if (!mbar_wait_warp(bar(L::bVFull + vs), (j / VST) & 1, abort_sig)) {
+          if (lane == 0) note_timeout(a.dev_status, kSiteVFull);
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t pa = tmem + (j % kNumS) * 128;  // P(j) over S(j)
-        const uint32_t vb = v_lo + vs * (L::kVBytes >> 4);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          umma_ts_lohi(tmem + kColO, pa + 8 * kk, vb + ((kk & 3) * 32 >> 4), desc_hi, kIdPV,
-                       (j > 0 || kk > 0));
+        const uint32_t pa = tmem + kColS + g * 128;   // P(j) over S(j)
+        const uint32_t od = tmem + kColO + g * 128;   // this group's O
+        const uint64_t vb = v0 + static_cast<uint64_t>(vs * (L::kVBytes >> 4));
+        umma_ts_x4_elect(od, pa, vb, vb + 2, vb + 4, vb + 6, kIdPV, j >= 2);
         if (2 * j + 1 < n_entries) {
-#pragma unroll
-          for (int kk = 4; kk < 8; ++kk)
-            umma_ts_lohi(tmem + kColO, pa + 8 * kk,
-                         vb + ((L::kVHalf + (kk & 3) * 32) >> 4), desc_hi, kIdPV, 1u);
+          const uint64_t vh = vb + (L::kVHalf >> 4);
+          umma_ts_x4_elect(od, pa + 32, vh, vh + 2, vh + 4, vh + 6, kIdPV, 1u);
         }
-        umma_commit(bar(L::bOReady + (j & 1)));
-        // S[j%3] now belongs to QK(j+3): PV(j), the last reader of P(j), was
-        // issued just before, and the tensor pipe runs this thread's MMAs in
-        // order.
-        if (j + kNumS < n_steps && !issue_qk(j + kNumS)) { ok = false; break; }
+        umma_commit_elect(bar(L::bOReady + g));
+        // S[g] now belongs to QK(j+2): PV(j), the last reader of P(j), was
+        // issued just before, and the tensor pipe runs the MMAs in order.
+        if (j + 2 < n_steps && !issue_qk(j + 2)) { ok = false; break; }
       }
-      if (!ok) {
+      if (!ok && lane == 0) {
         *abort_flag = 1;
         set_status(a.dev_status, SA_DEV_TIMEOUT);
       }
       // Every MMA issued above completes before TMEM is released.
-      umma_commit(bar(L::bFin));
-      mbar_wait(bar(L::bFin), 0, drain_sig);
+      umma_commit_elect(bar(L::bFin));
+      mbar_wait_warp(bar(L::bFin), 0, drain_sig);
     }
   } else {
     // ------------------------------------------------------------- softmax
-    // Two threads per row: `half` 0 owns the step's first key block and O
-    // columns [0, D/2); `half` 1 the second block and O columns [D/2, D).
-    // The pair meets at named barrier 1 + quarter every step, so a thread
-    // that gives up on a wait keeps looping (skipping all waits and TMEM
-    // work) to keep the pair's barrier counts equal.
-    const int quarter = warp & 3, half = warp >> 2;
+    const int grp = warp >> 2;                 // 0: even steps, 1: odd steps
+    const int quarter = warp & 3;
     const int r = quarter * 32 + lane;         // tile row == TMEM lane
     const int qh = r >> 6;                     // query block of this row (warp-uniform)
     const int t = qb0 * kBlock + r;            // query token
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const uint32_t s_col = kColS + grp * 128;
+    const uint32_t o_col = kColO + grp * 128;
     const int last_valid = S - (Nb - 1) * kBlock;  // tokens in the last block
     const float cl2 = a.scale_log2;
-    float* red = reinterpret_cast<float*>(smem + L::kRed);
-    float* lred = reinterpret_cast<float*>(smem + L::kLRed);
-    const uint32_t pair_bar = 1 + quarter;
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
 
-    for (int j = 0; j < n_steps; ++j) {
-      if (ok && !mbar_wait_warp(bar(L::bSFull + j % kNumS), (j / kNumS) & 1, abort_sig)) {
+    for (int j = grp; j < n_steps; j += 2) {
+      if (!mbar_wait_warp(bar(L::bSFull + grp), (j >> 1) & 1, abort_sig)) {
         ok = false;
         if (lane == 0) note_timeout(a.dev_status, kSiteSFull);
+        break;
       }
-      if (ok) tc_fence_after();
-      const int nblk = (2 * j + 1 < n_entries) ? 2 : 1;
-      const bool present = half == 0 || nblk == 2;
-      const uint32_t e = present ? info[2 * j + half] : 0u;
-      const bool mem = ok && present && ((e >> qh) & 1u);
-      const uint32_t s_col = (j % kNumS) * 128;
-
-      uint32_t sr[64];
-      float my_max = -INFINITY;
-      if (mem) {
-        tmem_ld32(lane_base + s_col + 64 * half, sr);
-        tmem_ld32(lane_base + s_col + 64 * half + 32, sr + 32);
-        tmem_wait_ld();
-        if (static_cast<int>(e >> 2) == Nb - 1) {  // ragged last block: keys past S weigh 0
-#pragma unroll
-          for (int u = 0; u < 64; ++u)
-            if (u >= last_valid) sr[u] = __float_as_uint(-INFINITY);
-        }
-        my_max = max64(sr);
-      }
-      float* slot = red + (j & 1) * 2 * BM;
-      slot[half * BM + r] = my_max;
-      // the partner's S loads are ordered before this thread's P stores,
-      // which overwrite S columns 32-63 of the partner's half
-      tc_fence_before();
-      named_bar_sync(pair_bar, 64);
       tc_fence_after();
-      const float mx = fmaxf(my_max, slot[(half ^ 1) * BM + r]);
-      if (!ok) continue;
+      const int nblk = (2 * j + 1 < n_entries) ? 2 : 1;
+      const uint32_t e0 = info[2 * j];
+      const uint32_t e1 = nblk == 2 ? info[2 * j + 1] : 0u;
+      const bool mem0 = (e0 >> qh) & 1u;
+      const bool mem1 = nblk == 2 && ((e1 >> qh) & 1u);
+
+      uint32_t sr[BN];
+      if (mem0) {
+        tmem_ld32(lane_base + s_col, sr);
+        tmem_ld32(lane_base + s_col + 32, sr + 32);
+      }
+      if (mem1) {
+        tmem_ld32(lane_base + s_col + 64, sr + 64);
+        tmem_ld32(lane_base + s_col + 96, sr + 96);
+      }
+      tmem_wait_ld();
+      // the ragged last block: keys past S weigh exactly zero
+      if (mem0 && static_cast<int>(e0 >> 2) == Nb - 1) {
+#pragma unroll
+        for (int u = 0; u < 64; ++u)
+          if (u >= last_valid) sr[u] = __float_as_uint(-INFINITY);
+      }
+      if (mem1 && static_cast<int>(e1 >> 2) == Nb - 1) {
+#pragma unroll
+        for (int u = 0; u < 64; ++u)
+          if (u >= last_valid) sr[64 + u] = __float_as_uint(-INFINITY);
+      }
+      float mx = -INFINITY;
+      if (mem0) mx = fmaxf(mx, max64(sr));
+      if (mem1) mx = fmaxf(mx, max64(sr + 64));
       const float bmax = mx * cl2;           // the scale is positive: max commutes
       float m_new = m_run;
       if (bmax > m_run + kRescaleLog2) m_new = bmax;  // also the first finite block
       const bool rescale = (m_new != m_run) && (m_run != -INFINITY);
       const float alpha = (m_new == m_run) ? 1.f : fast_exp2(m_run - m_new);
+      const float negm = -m_new;
       // P(j) over the consumed S(j) columns: keys 0-63 -> columns 0-31,
-      // keys 64-127 -> columns 32-63 (two fp16 per column).
+      // keys 64-127 -> columns 32-63 (two fp16 per column); each half is
+      // stored as soon as it is ready.
       float rs = 0.f;
-      if (present) {
+      {
         uint32_t pk[32];
-        if (mem) rs = exp_pack64(sr, cl2, -m_new, pk);
+        if (mem0) rs += exp_pack64(sr, cl2, negm, pk);
         else {
 #pragma unroll
           for (int u = 0; u < 32; ++u) pk[u] = 0u;
         }
-        tmem_st32(lane_base + s_col + 32 * half, pk);
+        tmem_st32(lane_base + s_col, pk);
+      }
+      if (nblk == 2) {
+        uint32_t pk[32];
+        if (mem1) rs += exp_pack64(sr + 64, cl2, negm, pk);
+        else {
+#pragma unroll
+          for (int u = 0; u < 32; ++u) pk[u] = 0u;
+        }
+        tmem_st32(lane_base + s_col + 32, pk);
       }
       l_run = l_run * alpha + rs;
       m_run = m_new;
       if (__any_sync(0xffffffffu, rescale)) {
-        // PV(j-1) must be done before O is scaled (j > 0 here: m_run was
-        // finite). S(j) ready implies PV(j-3) done (QK(j) was issued after
-        // it) and PV(j+1) is not yet issued, so on the barrier of PV(j-1)'s
-        // parity the phase of PV(j-1) is either the last completed or the
-        // pending one: no ambiguity.
-        if (!mbar_wait_warp(bar(L::bOReady + ((j - 1) & 1)), ((j - 1) >> 1) & 1, abort_sig)) {
-          ok = false;
-          if (lane == 0) note_timeout(a.dev_status, kSiteOReady);
-          continue;
-        }
-        tc_fence_after();
+        // S(j) ready means QK(j) is done, and QK(j) was issued after this
+        // group's previous PV(j-2): that PV is done too, and PV(j) waits for
+        // p_full(j), so O[grp] is stable here without another wait.
 #pragma unroll 1
-        for (int c = 0; c < D / 64; ++c) {
+        for (int c = 0; c < D / 32; ++c) {
           uint32_t o[32];
-          const uint32_t col = kColO + half * (D / 2) + 32 * c;
-          tmem_ld32(lane_base + col, o);
+          tmem_ld32(lane_base + o_col + 32 * c, o);
           tmem_wait_ld();
 #pragma unroll
           for (int u = 0; u < 32; ++u) o[u] = __float_as_uint(__uint_as_float(o[u]) * alpha);
-          tmem_st32(lane_base + col, o);
+          tmem_st32(lane_base + o_col + 32 * c, o);
         }
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(bar(L::bPFull + j % kNumS));
+      mbar_arrive(bar(L::bPFull + grp));
     }
     if (!ok) {
       *abort_flag = 1;
@@ -489,47 +513,67 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
 
     // ------------------------------------------------------------ epilogue
-    lred[half * BM + r] = l_run;
-    named_bar_sync(pair_bar, 64);
-    const float l_tot = l_run + lred[(half ^ 1) * BM + r];
+    // Merge the two groups' partial results for this row: both threads of
+    // the row (same lane, groups 0 and 1) swap (m, l) through shared memory,
+    // then each writes half of the output columns.
+    float* xch = reinterpret_cast<float*>(smem + L::kXch);
+    xch[(grp * 2 + 0) * BM + r] = m_run;
+    xch[(grp * 2 + 1) * BM + r] = l_run;
     bool have_o = ok && n_steps > 0;
     if (have_o) {
-      // The MMA thread commits bFin after its last PV; softmax need not have
-      // seen every o_ready phase, so that barrier's parity is no guide here.
+      // bFin completes when every MMA of the tile is done
       have_o = mbar_wait_warp(bar(L::bFin), 0, abort_sig);
       if (!have_o) {
         *abort_flag = 1;
         if (lane == 0) note_timeout(a.dev_status, kSiteFin);
       }
-      tc_fence_after();
     }
-    const bool row_ok = t < S;
+    tc_fence_before();
+    named_bar_sync(1 + quarter, 2 * 32);
+    tc_fence_after();
+    const float m0 = xch[0 * BM + r], l0 = xch[1 * BM + r];
+    const float m1 = xch[2 * BM + r], l1 = xch[3 * BM + r];
+    const float m = fmaxf(m0, m1);
+    const float s0 = l0 > 0.f ? fast_exp2(m0 - m) : 0.f;   // group 0's weight
+    const float s1 = l1 > 0.f ? fast_exp2(m1 - m) : 0.f;   // group 1's weight
+    const float l_tot = l0 * s0 + l1 * s1;
     const float inv_l = l_tot > 0.f ? 1.f / l_tot : 0.f;
+    const float w0 = s0 * inv_l, w1 = s1 * inv_l;
+    const bool row_ok = t < S;
     uint16_t* orow = a.o + b * a.os[0] + static_cast<int64_t>(t) * a.os[1] + h * a.os[2] +
-                     half * (D / 2);
-    uint32_t o[D / 2];
-    if (have_o) {
+                     grp * (D / 2);
 #pragma unroll
-      for (int c = 0; c < D / 64; ++c)
-        tmem_ld32(lane_base + kColO + half * (D / 2) + 32 * c, o + 32 * c);
-      tmem_wait_ld();
-    } else {
+    for (int c = 0; c < D / 64; ++c) {
+      const uint32_t col = grp * (D / 2) + 32 * c;
+      uint32_t oa[32], ob[32];
+      if (have_o) {
+        tmem_ld32(lane_base + kColO + col, oa);
+        tmem_ld32(lane_base + kColO + 128 + col, ob);
+        tmem_wait_ld();
+      }
+      if (row_ok) {
 #pragma unroll
-      for (int u = 0; u < D / 2; ++u) o[u] = 0u;
-    }
-    if (row_ok) {
+        for (int v = 0; v < 4; ++v) {
+          float f[8];
 #pragma unroll
-      for (int v = 0; v < D / 16; ++v) {
-        uint4 w;
-        w.x = pack_bf162(__uint_as_float(o[8 * v + 0]) * inv_l, __uint_as_float(o[8 * v + 1]) * inv_l);
-        w.y = pack_bf162(__uint_as_float(o[8 * v + 2]) * inv_l, __uint_as_float(o[8 * v + 3]) * inv_l);
-        w.z = pack_bf162(__uint_as_float(o[8 * v + 4]) * inv_l, __uint_as_float(o[8 * v + 5]) * inv_l);
-        w.w = pack_bf162(__uint_as_float(o[8 * v + 6]) * inv_l, __uint_as_float(o[8 * v + 7]) * inv_l);
-        *reinterpret_cast<uint4*>(orow + 8 * v) = w;
+          for (int u = 0; u < 8; ++u) {
+            // a group with no weight may never have written its O: select,
+            // never multiply, so stale TMEM cannot leak in as NaN
+            const float xa = (have_o && s0 > 0.f) ? __uint_as_float(oa[8 * v + u]) * w0 : 0.f;
+            const float xb = (have_o && s1 > 0.f) ? __uint_as_float(ob[8 * v + u]) * w1 : 0.f;
+            f[u] = xa + xb;
+          }
+          uint4 wv;
+          wv.x = pack_bf162(f[0], f[1]);
+          wv.y = pack_bf162(f[2], f[3]);
+          wv.z = pack_bf162(f[4], f[5]);
+          wv.w = pack_bf162(f[6], f[7]);
+          *reinterpret_cast<uint4*>(orow + 32 * c + 8 * v) = wv;
+        }
       }
     }
-    if (row_ok && half == 0 && a.lse) {
-      const float lse = l_tot > 0.f ? m_run * 0.69314718055994531f + logf(l_tot) : -INFINITY;
+    if (row_ok && grp == 0 && a.lse) {
+      const float lse = l_tot > 0.f ? m * 0.69314718055994531f + logf(l_tot) : -INFINITY;
       a.lse[(static_cast<int64_t>(b) * a.H + h) * S + t] = lse;
     }
   }

@@ -202,6 +202,95 @@ __device__ __forceinline__ void umma_ts_lohi(uint32_t d_tmem, uint32_t a_tmem, u
       : "memory");
 }
 
+// Four MMAs back to back into one accumulator (consecutive K slices), all
+// descriptors computed beforehand: issuing costs the four instructions only.
+// The first MMA overwrites D unless `accumulate` is set; the rest accumulate.
+__device__ __forceinline__ void umma_ss_x4(uint32_t d_tmem, uint64_t a0, uint64_t a1, uint64_t a2,
+                                           uint64_t a3, uint64_t b0, uint64_t b1, uint64_t b2,
+                                           uint64_t b3, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, t;\n\t"
+      "setp.ne.b32 p, %10, 0;\n\t"
+      "setp.eq.b32 t, %10, %10;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %5, %9, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %2, %6, %9, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %7, %9, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %4, %8, %9, t;\n\t}"
+      ::"r"(d_tmem), "l"(a0), "l"(a1), "l"(a2), "l"(a3), "l"(b0), "l"(b1), "l"(b2), "l"(b3),
+        "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Four TS MMAs (A from TMEM columns a, a+8, a+16, a+24) back to back.
+__device__ __forceinline__ void umma_ts_x4(uint32_t d_tmem, uint32_t a_tmem, uint64_t b0,
+                                           uint64_t b1, uint64_t b2, uint64_t b3, uint32_t idesc,
+                                           uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, t;\n\t.reg .b32 a1, a2, a3;\n\t"
+      "setp.ne.b32 p, %7, 0;\n\t"
+      "setp.eq.b32 t, %7, %7;\n\t"
+      "add.u32 a1, %1, 8;\n\t"
+      "add.u32 a2, %1, 16;\n\t"
+      "add.u32 a3, %1, 24;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %6, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], %3, %6, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a2], %4, %6, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a3], %5, %6, t;\n\t}"
+      ::"r"(d_tmem), "r"(a_tmem), "l"(b0), "l"(b1), "l"(b2), "l"(b3), "r"(idesc),
+        "r"(accumulate)
+      : "memory");
+}
+
+// The issuing forms used by a converged warp: every lane executes them and
+// elect.sync picks one lane to issue. Issued this way, back-to-back MMAs run
+// at the tensor pipe's rate; issued by a lone lane of a diverged warp, each
+// batch pays tens of cycles of issue overhead.
+__device__ __forceinline__ void umma_ss_x4_elect(uint32_t d_tmem, uint64_t a0, uint64_t a1,
+                                                 uint64_t a2, uint64_t a3, uint64_t b0,
+                                                 uint64_t b1, uint64_t b2, uint64_t b3,
+                                                 uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p, t;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %10, 0;\n\t"
+      "setp.eq.b32 t, %10, %10;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %5, %9, p;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %2, %6, %9, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %7, %9, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %4, %8, %9, t;\n\t}"
+      ::"r"(d_tmem), "l"(a0), "l"(a1), "l"(a2), "l"(a3), "l"(b0), "l"(b1), "l"(b2), "l"(b3),
+        "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void umma_ts_x4_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t b0,
+                                                 uint64_t b1, uint64_t b2, uint64_t b3,
+                                                 uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p, t;\n\t.reg .b32 a1, a2, a3;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %7, 0;\n\t"
+      "setp.eq.b32 t, %7, %7;\n\t"
+      "add.u32 a1, %1, 8;\n\t"
+      "add.u32 a2, %1, 16;\n\t"
+      "add.u32 a3, %1, 24;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %6, p;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], %3, %6, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a2], %4, %6, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a3], %5, %6, t;\n\t}"
+      ::"r"(d_tmem), "r"(a_tmem), "l"(b0), "l"(b1), "l"(b2), "l"(b3), "r"(idesc),
+        "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void umma_commit_elect(uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}"
+      ::"r"(bar) : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05.mma this thread issued so far is done.
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
   asm volatile(

@@ -48,9 +48,19 @@ constexpr int BN = 128;   // key rows per step (two key blocks)
 // PV(j) done (o_ready[j%2]) frees V stage j%2, so the producers wait on those.
 constexpr int KST = 2;
 constexpr int VST = 2;
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;   // three warpgroups: softmax 0, softmax 1, producer + MMA
 constexpr int kGroupThreads = 128;
-constexpr int kProducerWarp = 8, kMmaWarp = 9;
+constexpr int kProducerWarp = 8, kMmaWarp = 9;   // warps 10, 11 only join the barriers
+// Register split (setmaxnreg). At launch ptxas gives every thread
+// kLaunchRegs (65536 / 384 rounded down to a multiple of 8); the two softmax
+// warpgroups then grow to kSoftmaxRegs and the producer/MMA warpgroup shrinks
+// to kControlRegs: 2*128*216 + 128*64 = 63,488 <= 384*168 = 64,512, and per
+// SM sub-partition (one warp of each warpgroup) 216 + 216 + 64 <= 512.
+constexpr int kLaunchRegs = 168;
+constexpr int kSoftmaxRegs = 216;
+constexpr int kControlRegs = 64;
+static_assert(2 * 128 * kSoftmaxRegs + 128 * kControlRegs <= kThreads * kLaunchRegs,
+              "register split exceeds the launch allocation");
 constexpr int kTmemCols = 512;
 constexpr int kColS = 0;      // S[g] at columns [128 g, 128 g + 128)
 constexpr int kColO = 256;    // O[g] at columns [256 + 128 g, 256 + 128 g + D)
@@ -270,7 +280,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   const int n_entries = static_cast<int>(misc[2]);
   const int n_steps = (n_entries + 1) >> 1;
 
+  // Each role branch resizes its registers first thing and does not rejoin
+  // the others before the final barrier, so ptxas can give each branch its
+  // own budget.
   if (warp == kProducerWarp) {
+    regs_dec<kControlRegs>();
     // ------------------------------------------------------------ producer
     // Lane 0 streams Q and then K, lane 1 streams V, each as far ahead as its
     // ring allows, so a K load never waits behind a V stage or vice versa.
@@ -329,6 +343,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         if (issued[s2]) mbar_wait(bar(L::bVFull + s2), (issued[s2] - 1) & 1, drain_sig);
     }
   } else if (warp == kMmaWarp) {
+    regs_dec<kControlRegs>();
     // ----------------------------------------------------------------- MMA
     // The whole warp runs this loop in step (warp-uniform waits); elect.sync
     // picks the lane that issues each batch of MMAs and each commit.
@@ -407,7 +422,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       umma_commit_elect(bar(L::bFin));
       mbar_wait_warp(bar(L::bFin), 0, drain_sig);
     }
+  } else if (warp > kMmaWarp) {
+    regs_dec<kControlRegs>();   // warps 10 and 11: nothing to do but the barriers
   } else {
+    regs_inc<kSoftmaxRegs>();
     // ------------------------------------------------------------- softmax
     const int grp = warp >> 2;                 // 0: even steps, 1: odd steps
     const int quarter = warp & 3;

@@ -368,6 +368,18 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+// Warpgroup register reallocation: every warp of a warpgroup executes the
+// same one. `inc` waits until the pool the CTA was launched with can cover it,
+// so the warpgroups' new sizes must add up to at most that launch total.
+template <uint32_t N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ------------------------------------------------------------ named barrier
 
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {

@@ -94,8 +94,13 @@ sa_status encode_vt(CUtensorMap* m, const void* base, const sa_params* p) {
   return r == CUDA_SUCCESS ? SA_OK : SA_ERR_INVALID_ARG;
 }
 
-size_t attn_ws_bytes(const sa_params* p) {
+size_t vt_bytes(const sa_params* p) {
   return static_cast<size_t>(p->B) * p->H * p->D * s_pad_of(p->S) * 2;
+}
+
+// V repacked to fp16, then (256-byte aligned) the persistent kernel's tile counter.
+size_t attn_ws_bytes(const sa_params* p) {
+  return ((vt_bytes(p) + 255) & ~static_cast<size_t>(255)) + 256;
 }
 
 sa_status attn_common(const sa_params* p, const void* q, const void* k, const void* v,
@@ -138,6 +143,10 @@ sa_status attn_common(const sa_params* p, const void* q, const void* k, const vo
   a.Nb = Nb;
   a.n_pairs = (Nb + 1) / 2;
   a.scale_log2 = static_cast<float>(scale64_of(p) * 1.4426950408889634);
+  a.n_tiles = p->B * p->H * a.n_pairs;
+  a.tile_counter = reinterpret_cast<int*>(static_cast<char*>(ws) +
+                                          ((vt_bytes(p) + 255) & ~static_cast<size_t>(255)));
+  if (cudaMemsetAsync(a.tile_counter, 0, sizeof(int), st) != cudaSuccess) return SA_ERR_CUDA;
   return from_cuda(launch_attn(p->D, maps, a, st));
 }
 

@@ -59,6 +59,8 @@ struct AttnArgs {
   int64_t os[3];
   int B, S, H, Nb, n_pairs;
   float scale_log2;        // softmax_scale * log2(e)
+  int* tile_counter;       // zeroed before the launch; tiles are taken in order
+  int n_tiles;             // B * H * n_pairs
 };
 
 struct AttnMaps {

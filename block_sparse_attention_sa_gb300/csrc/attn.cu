@@ -142,41 +142,42 @@ __device__ __forceinline__ void note_timeout(int32_t* st, int site) {
   set_status(st, SA_DEV_TIMEOUT | (1 << (8 + site)));
 }
 
-// max over 64 fp32 values (bit patterns), eight independent chains.
+// max over 64 fp32 values (bit patterns): eight chains of three-input max.
 __device__ __forceinline__ float max64(const uint32_t* v) {
   float m[8];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) m[i] = __uint_as_float(v[i]);
+  for (int i = 0; i < 8; ++i) m[i] = fmaxf(__uint_as_float(v[i]), __uint_as_float(v[8 + i]));
 #pragma unroll
-  for (int i = 8; i < 64; ++i) m[i & 7] = fmaxf(m[i & 7], __uint_as_float(v[i]));
+  for (int i = 16; i < 64; i += 16)
 #pragma unroll
-  for (int w = 4; w >= 1; w >>= 1)
-#pragma unroll
-    for (int i = 0; i < w; ++i) m[i] = fmaxf(m[i], m[i + w]);
-  return m[0];
+    for (int c = 0; c < 8; ++c)
+      m[c] = fmax3(m[c], __uint_as_float(v[i + c]), __uint_as_float(v[i + 8 + c]));
+  return fmaxf(fmax3(m[0], m[1], m[2]), fmax3(fmax3(m[3], m[4], m[5]), m[6], m[7]));
 }
 
 // p = 2^(s * c - m) for 64 logits, packed as fp16 pairs into 32 words;
-// returns the fp32 sum of the p (eight independent chains).
+// returns the fp32 sum of the p. The scale-and-subtract and the running sums
+// use paired fp32 arithmetic (four independent sum chains).
 __device__ __forceinline__ float exp_pack64(const uint32_t* v, float c, float negm,
                                             uint32_t* pk) {
-  float acc[8];
+  const uint64_t c2 = f2_pack(c, c), m2 = f2_pack(negm, negm);
+  uint64_t acc[4];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+  for (int i = 0; i < 4; ++i) acc[i] = 0ull;
 #pragma unroll
   for (int u = 0; u < 64; u += 2) {
-    const float p0 = fast_exp2(fmaf(__uint_as_float(v[u]), c, negm));
-    const float p1 = fast_exp2(fmaf(__uint_as_float(v[u + 1]), c, negm));
-    acc[(u >> 1) & 7] += p0 + p1;
+    const uint64_t y = f2_fma(f2_pack(__uint_as_float(v[u]), __uint_as_float(v[u + 1])), c2, m2);
+    float y0, y1;
+    f2_unpack(y, y0, y1);
+    const float p0 = fast_exp2(y0), p1 = fast_exp2(y1);
+    acc[(u >> 1) & 3] = f2_add(acc[(u >> 1) & 3], f2_pack(p0, p1));
     pk[u >> 1] = pack_half2(p0, p1);
   }
-#pragma unroll
-  for (int w = 4; w >= 1; w >>= 1)
-#pragma unroll
-    for (int i = 0; i < w; ++i) acc[i] += acc[i + w];
-  return acc[0];
+  const uint64_t t = f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3]));
+  float lo, hi;
+  f2_unpack(t, lo, hi);
+  return lo + hi;
 }
-
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)

@@ -162,16 +162,32 @@ __global__ void __launch_bounds__(256) score_kernel(RouteArgs a) {
     Ks[lc + 0][lr] = ka.x; Ks[lc + 1][lr] = ka.y; Ks[lc + 2][lr] = ka.z; Ks[lc + 3][lr] = ka.w;
     Ks[lc + 4][lr] = kb4.x; Ks[lc + 5][lr] = kb4.y; Ks[lc + 6][lr] = kb4.z; Ks[lc + 7][lr] = kb4.w;
     __syncthreads();
-#pragma unroll 8
-    for (int kk = 0; kk < KC; ++kk) {
-      const float4 qv = *reinterpret_cast<const float4*>(&Qs[kk][ty * 4]);
-      const float4 kv = *reinterpret_cast<const float4*>(&Ks[kk][tx * 4]);
-      const float qr[4] = {qv.x, qv.y, qv.z, qv.w};
-      const float kc[4] = {kv.x, kv.y, kv.z, kv.w};
+    // Each chunk of 32 dims is summed as two fresh 16-term FMA chains that
+    // are then added to the running total: the rounding error of a score is
+    // then bounded by gamma_{16 + D/16 + 3} (not gamma_{D + 3} of a single
+    // chain), which keeps the fp64 recheck band narrow.
+#pragma unroll
+    for (int hh = 0; hh < KC; hh += 16) {
+      float t[4][4];
 #pragma unroll
       for (int r = 0; r < 4; ++r)
 #pragma unroll
-        for (int c = 0; c < 4; ++c) acc[r][c] = fmaf(qr[r], kc[c], acc[r][c]);
+        for (int c = 0; c < 4; ++c) t[r][c] = 0.f;
+#pragma unroll 8
+      for (int kk = hh; kk < hh + 16; ++kk) {
+        const float4 qv = *reinterpret_cast<const float4*>(&Qs[kk][ty * 4]);
+        const float4 kv = *reinterpret_cast<const float4*>(&Ks[kk][tx * 4]);
+        const float qr[4] = {qv.x, qv.y, qv.z, qv.w};
+        const float kc[4] = {kv.x, kv.y, kv.z, kv.w};
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+          for (int c = 0; c < 4; ++c) t[r][c] = fmaf(qr[r], kc[c], t[r][c]);
+      }
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[r][c] += t[r][c];
     }
   }
 
@@ -248,7 +264,11 @@ __global__ void __launch_bounds__(256) select_kernel(RouteArgs a) {
     const float kmx = __int_as_float(ws_ptr<int>(a.ws, a.L.kmax)[bh]);
     const float* kn = ws_ptr<float>(a.ws, a.L.knorm) + static_cast<size_t>(bh) * a.Nb;
     const float gq = a.gamma * a.scale * qn;
-    const float err_row = gq * kmx + 1e-5f * (1.f + fabsf(T));
+    // T carries the worst logit error (the max over k of the bound above)
+    // plus the roundings of the log-sum-exp itself: expf (2 ulp) and the
+    // short shuffle-tree sums (relative 1e-6 of Z, so 1e-6 absolute in log Z),
+    // logf (1 ulp of |log Z| <= 8) and three additions (ulps of |T|).
+    const float err_row = gq * kmx + 2e-6f + 5e-7f * fabsf(T);
     const float* srow = ws_ptr<float>(a.ws, a.L.scores) + row * a.Nb;
     for (int w = 0; w < a.words; ++w) {
       const int j = w * 32 + lane;

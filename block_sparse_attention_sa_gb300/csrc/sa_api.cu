@@ -237,9 +237,11 @@ sa_status sa_route(const sa_params* p, const void* q, const void* k, int32_t* ro
   a.log_tau_over_nb = a.keep_all ? 0.f
                                  : static_cast<float>(std::log(static_cast<double>(p->tau)) -
                                                       std::log(static_cast<double>(L.Nb)));
-  // gamma_{D+3} (1 + 1%) with u = 2^-24: bounds the fp32 pooled dot product
-  // error by gamma * scale * |qbar| |kbar|.
-  const double u = std::ldexp(1.0, -24), n = p->D + 3;
+  // gamma_n (1 + 1%) with u = 2^-24 and n = 16 + D/16 + 3: the score kernel
+  // sums each dot product as 16-term FMA chains added into a running total,
+  // after rounding qbar, kbar to fp32 and before scaling, so the fp32 score
+  // error is at most gamma * scale * |qbar| |kbar| (Cauchy-Schwarz).
+  const double u = std::ldexp(1.0, -24), n = 16 + p->D / 16 + 3;
   a.gamma = static_cast<float>(1.01 * n * u / (1.0 - n * u));
   a.ws = static_cast<char*>(workspace);
   a.L = L;

@@ -89,6 +89,18 @@ def barrier(world: int):
         dist.barrier()
 
 
+def whole_job_tflops(flops_per_rank: int, ms_per_step: float, world: int) -> float:
+    """Aggregate throughput of ``world`` replicas that each process
+    ``flops_per_rank`` per step, timed by the slowest rank (``ms_per_step`` is
+    already the max over ranks)."""
+    return world * flops_per_rank / (ms_per_step * 1e-3) / 1e12
+
+
+def timed_max_ms(local_ms: float, steps: int, world: int, device=None) -> float:
+    """Per-step time of the job: the slowest rank's timed region / steps."""
+    return reduce_max(local_ms, world, device) / steps
+
+
 class ClockSampler:
     """nvidia-smi clock/throttle samples while the timed region runs."""
 
@@ -228,11 +240,11 @@ def run_ours(args):
         torch.cuda.synchronize()
     barrier(world)
     sa.check_dev_status(status, "bench")
-    total_ms = reduce_max(start.elapsed_time(end), world, dev)
+    ms_step = timed_max_ms(start.elapsed_time(end), args.steps, world, dev)
+    total_ms = ms_step * args.steps
     route_ms = [e[0].elapsed_time(e[1]) for e in evs]
     attn_ms = [e[1].elapsed_time(e[2]) for e in evs]
-    ms_step = total_ms / args.steps
-    value = world * flops / (ms_step * 1e-3) / 1e12
+    value = whole_job_tflops(flops, ms_step, world)
     attn_avg = statistics.mean(attn_ms)
     burst, sustained, _, peak_src = measured_peaks()
     long_region = total_ms > 1000.0
@@ -292,9 +304,9 @@ def run_e2e(sa, cfg, q, k, v, bufs, flops, args, world, dev, stream):
         sa.sa_forward_host(qh, kh, vh, cfg.P, cfg.tau, bufs=bufs, o_host=oh)
     e.record(stream)
     torch.cuda.synchronize()
-    ms = reduce_max(s.elapsed_time(e), world, dev) / steps
+    ms = timed_max_ms(s.elapsed_time(e), steps, world, dev)
     nbytes = q.numel() * 2
-    return {"value": round(world * flops / (ms * 1e-3) / 1e12, 2), "unit": UNIT,
+    return {"value": round(whole_job_tflops(flops, ms, world), 2), "unit": UNIT,
             "ms_per_step": round(ms, 4), "h2d_bytes_per_step": 3 * nbytes,
             "d2h_bytes_per_step": nbytes}
 

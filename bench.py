@@ -47,9 +47,10 @@ UNIT = "TFLOP/s"
 KERNELS_PER_STEP = 8  # pool, score, select, recheck, scan, emit, pack_v, attention
 
 # DRAM traffic of one attention-kernel launch at the release workload, from
-# the ncu capture summarised under profiles/, valid only for the attn.cu it
-# was taken on (sha256 prefix).
-ATTN_TRAFFIC = {"bytes": None, "attn_cu_sha256": None}
+# the ncu capture summarised under profiles/ (taken with 8 of the 56 heads and
+# scaled by 7: the traffic grows with the heads processed), valid only for the
+# attn.cu it was taken on (sha256 prefix); otherwise reported as null.
+ATTN_TRAFFIC = {"bytes": 2.187e9, "attn_cu_sha256": "6f778c3a18ba103f"}
 
 
 def file_sha(path):

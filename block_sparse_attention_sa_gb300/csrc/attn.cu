@@ -17,25 +17,32 @@
 // Persistent CTAs. One CTA per SM takes tiles from a global counter in
 // (batch, head, pair) order, so concurrently running tiles share a head's
 // K/V in L2. While one tile runs, a planner warp builds the next tile's key
-// walk into the other half of a double buffer, the producer loads the next
-// Q as soon as the last QK of the tile has read the old one, and the MMA
-// warp queues the next tile's QKs during the current tile's epilogue.
+// walk into the other half of a double buffer, and the next tile's first
+// QK^T products are computed during the current tile's epilogue.
 //
-// Split-K ping-pong. A tile's steps alternate between two softmax
-// warpgroups: group 0 takes the even steps, group 1 the odd ones. Each group
-// has its own S buffer, running max and sum, and O accumulator in TMEM
-// (S0 S1 O0 O1 = 4 x 128 columns), so one group's softmax runs while the
-// tensor pipe works on the other group's QK^T and PV. The two partial
-// results are merged once per tile (rescaled to the common max, summed,
-// divided by the common sum).
+// Pipeline. TMEM holds three S buffers and one O accumulator (3 x 128 + D
+// columns). Step j's S = Q K(j)^T (bf16 x bf16 -> fp32) goes to buffer j % 3;
+// the softmax turns it into P (fp16) over the same columns; O += P V(j)
+// (fp16, A from TMEM). The MMA warp issues QK^T(j+2) before it waits for
+// P(j) -- its buffer last held step j-1, whose PV was issued already -- so
+// the tensor pipe has the next products queued while the softmax works and
+// the softmax always finds its next S ready: the step rate is set by the
+// slower of the tensor pipe and the softmax, not by their sum.
 //
-// Warps: 0-3 softmax group 0, 4-7 softmax group 1 (one thread per row =
-// TMEM lane), 8 producer (lane 0: Q and K, lane 1: V), 9 MMA (converged;
-// elect.sync issues), 10 planner, 11 idle. Step j: K(j) -> S[j%2] = Q K^T
-// (bf16 x bf16 -> fp32) -> softmax(j) reads S, writes P (fp16) over the same
-// columns -> O[j%2] += P V (fp16, A from TMEM) -> QK^T(j+2) reuses S[j%2].
-// No data-dependent load sits inside a pipelined loop: the walk is built
-// ahead by the planner. Every wait is bounded (SA_DEV_TIMEOUT) and an
+// Softmax. Eight warps; the two threads of a row (warps q and q+4 share
+// TMEM lane quarter q) take one 64-key block of the step each. They agree on
+// the row's running max through shared memory and a named barrier for the
+// pair, keep their own partial row sums, and each rescales and writes its
+// half of O's columns. The running max moves only when a block max exceeds
+// it by more than 2^14 (then O is rescaled, after the last PV into it has
+// completed).
+//
+// Warps: 0-7 softmax, 8 producer (Q, and K and V through one ring of
+// stages in the order the MMA warp consumes them), 9 MMA (converged;
+// elect.sync issues), 10 planner, 11 idle. No data-dependent load sits inside
+// a pipelined loop: the walk is built ahead by the planner. Every mbarrier
+// wait is bounded (SA_DEV_TIMEOUT); the softmax pairs carry a stop bit
+// through each exchange so both warps of a pair leave together, and an
 // aborted CTA drains its own copies and MMAs and frees TMEM before it exits.
 #include <cmath>
 #include <cuda_bf16.h>
@@ -50,25 +57,24 @@ namespace {
 
 constexpr int BM = 128;   // query rows per tile
 constexpr int BN = 128;   // key rows per step (two key blocks)
-constexpr int KST = 3;    // K stages
-constexpr int VST = 2;    // V stages
-constexpr int kThreads = 384;   // three warpgroups: softmax 0, softmax 1, control
-constexpr int kGroupThreads = 128;
+constexpr int KVST = 5;   // stages of the K/V ring (each holds one K or one V^T tile of a step)
+constexpr int kSBuf = 3;  // S buffers in TMEM
+constexpr int kThreads = 384;   // three warpgroups: softmax (two), control
 constexpr int kSoftmaxThreads = 256;
 constexpr int kProducerWarp = 8, kMmaWarp = 9, kPlannerWarp = 10;  // warp 11: barriers only
 // Register split (setmaxnreg). At launch ptxas gives every thread
 // kLaunchRegs (65536 / 384 rounded down to a multiple of 8); the two softmax
 // warpgroups then grow to kSoftmaxRegs and the control warpgroup shrinks
-// to kControlRegs: 2*128*216 + 128*64 = 63,488 <= 384*168 = 64,512, and per
-// SM sub-partition (one warp of each warpgroup) 216 + 216 + 64 <= 512.
+// to kControlRegs: 2*128*208 + 128*80 = 63,488 <= 384*168 = 64,512, and per
+// SM sub-partition (one warp of each warpgroup) 208 + 208 + 80 <= 512.
 constexpr int kLaunchRegs = 168;
-constexpr int kSoftmaxRegs = 216;
-constexpr int kControlRegs = 64;
+constexpr int kSoftmaxRegs = 208;
+constexpr int kControlRegs = 80;
 static_assert(2 * 128 * kSoftmaxRegs + 128 * kControlRegs <= kThreads * kLaunchRegs,
               "register split exceeds the launch allocation");
 constexpr int kTmemCols = 512;
-constexpr int kColS = 0;      // S[g] at columns [128 g, 128 g + 128)
-constexpr int kColO = 256;    // O[g] at columns [256 + 128 g, 256 + 128 g + D)
+constexpr int kColS = 0;      // S[b] at columns [128 b, 128 b + 128), b < kSBuf
+constexpr int kColO = 384;    // O at columns [384, 384 + D)
 // Lazy rescale: the running max moves only when a block max exceeds it by
 // more than 2^14, so P <= 16384 stays well inside fp16; values that fall
 // below fp16's normal range weigh under 2^-28 of the row max.
@@ -79,32 +85,28 @@ struct Smem {
   static constexpr int kRegion = BM * 128;            // one 64-wide K slice of 128 rows
   static constexpr int kQ = 0;
   static constexpr int kQBytes = BM * D * 2;
-  static constexpr int kK = kQ + kQBytes;
-  static constexpr int kKBytes = BN * D * 2;
-  static constexpr int kV = kK + KST * kKBytes;
-  static constexpr int kVBytes = BN * D * 2;
-  static constexpr int kVHalf = D * 128;              // one 64-key half of a V^T stage
-  static constexpr int kBar = kV + VST * kVBytes;
+  static constexpr int kStageBytes = BN * D * 2;      // one K tile or one V^T tile of a step
+  static constexpr int kKV = kQ + kQBytes;
+  static constexpr int kVHalf = D * 128;              // one 64-key half of a V^T tile
+  static constexpr int kBar = kKV + KVST * kStageBytes;
   // barriers (counts in the init loop below)
   static constexpr int bInfoFull = 0;                 // [2] planner wrote walk x
   static constexpr int bInfoEmpty = bInfoFull + 2;    // [2] every consumer is done with walk x
   static constexpr int bQFull = bInfoEmpty + 2;       // Q of the current tile landed
   static constexpr int bQEmpty = bQFull + 1;          // the tile's last QK is done with Q
-  static constexpr int bKFull = bQEmpty + 1;          // [KST]
-  static constexpr int bKEmpty = bKFull + KST;        // [KST]
-  static constexpr int bVFull = bKEmpty + KST;        // [VST]
-  static constexpr int bVEmpty = bVFull + VST;        // [VST]
-  static constexpr int bSFull = bVEmpty + VST;        // [2] QK of group g's step done
-  static constexpr int bPFull = bSFull + 2;           // [2] softmax of group g's step done
-  static constexpr int bTileDone = bPFull + 2;        // every PV of the tile done
-  static constexpr int bXch = bTileDone + 1;          // [2] both groups posted (m, l)
-  static constexpr int bOFree = bXch + 2;             // both groups have read O
+  static constexpr int bKVFull = bQEmpty + 1;         // [KVST] a stage landed
+  static constexpr int bKVEmpty = bKVFull + KVST;     // [KVST] its MMAs are done with a stage
+  static constexpr int bSFull = bKVEmpty + KVST;      // [kSBuf] QK into S[b] done
+  static constexpr int bPFull = bSFull + kSBuf;       // [kSBuf] softmax wrote P over S[b]
+  static constexpr int bPVDone = bPFull + kSBuf;      // one phase per PV: that PV is done
+  static constexpr int bTileDone = bPVDone + 1;       // every PV of the tile done
+  static constexpr int bOFree = bTileDone + 1;        // the epilogue has read O
   static constexpr int bFin = bOFree + 1;             // every MMA done (exit)
   static constexpr int kNumBars = bFin + 1;
   static constexpr int kMisc = kBar + kNumBars * 8;   // tmem base, abort flag
   static constexpr int kHdr = kMisc + 16;             // [2][4] walk headers: b, h, pair, n
-  static constexpr int kXch = kHdr + 32;              // [2 parity][2 groups][2 (m, l)][128]
-  static constexpr int kBits = kXch + 2 * 2 * 2 * BM * 4;
+  static constexpr int kXch = kHdr + 32;              // pair exchange: [2 slots][2 halves][BM] x 2 words
+  static constexpr int kBits = kXch + 2 * 2 * BM * 8;
   static constexpr int kInfo = kBits + 2 * (kMaxNbAttn / 32) * 4;  // [2][kMaxNbAttn] walks
   static constexpr int kEnd = kInfo + 2 * kMaxNbAttn * 2;
   static constexpr int kBytes = kEnd + 1024;          // slack to align the base to 1 KB
@@ -127,8 +129,8 @@ __device__ __forceinline__ void set_status(int32_t* st, int bits) {
 // Wait sites, recorded as bit (8 + site) next to SA_DEV_TIMEOUT when a wait
 // gives up, so a status word names the stage that stalled.
 enum WaitSite {
-  kSiteKStage = 0, kSiteVStage, kSiteQFull, kSiteKFull, kSitePFull, kSiteVFull,
-  kSiteSFull, kSiteFin, kSiteInfo, kSiteOFree
+  kSiteKVStage = 0, kSiteQFull, kSiteKVFull, kSitePFull, kSiteSFull, kSiteFin, kSiteInfo,
+  kSiteOFree, kSitePVDone
 };
 
 __device__ __forceinline__ bool elect_one() {
@@ -179,6 +181,15 @@ __device__ __forceinline__ float exp_pack64(const uint32_t* v, float c, float ne
   return lo + hi;
 }
 
+// The ragged last key block: logits of keys past S become -inf (weight 0).
+__device__ __forceinline__ void mask_tail(uint32_t* v, uint32_t entry, int Nb, int last_valid) {
+  if (static_cast<int>(entry >> 2) == Nb - 1) {
+#pragma unroll
+    for (int u = 0; u < 64; ++u)
+      if (u >= last_valid) v[u] = __float_as_uint(-INFINITY);
+  }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -210,15 +221,17 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     // Arrival counts. No barrier can complete its next phase before each of
     // its waiters has seen the current one, so parity waits never fall a
     // full round behind: every next phase needs work the waiter releases
-    // after its wait (the walk buffers need all their consumers; QK(j+2)
-    // follows p_full(j); a stage is refilled only after it was freed; the
-    // next tile's first PV waits for o_free, which needs every softmax
-    // thread past its tile_done wait; and so on).
+    // after its wait (the walk buffers need all their consumers; a ring
+    // stage is refilled only after its MMAs freed it, and they wait for it
+    // to fill; QK into S[b] again needs the PV that read P(b), which waits
+    // for p_full; a PV-done phase needs a PV, which needs the softmax's
+    // p_full; the next tile's first PV waits for o_free, which needs every
+    // softmax thread past its tile_done wait; and so on).
     for (int i = 0; i < L::kNumBars; ++i) {
       uint32_t cnt = 1;
-      if (i == L::bInfoEmpty || i == L::bInfoEmpty + 1) cnt = 3 + kSoftmaxThreads;
-      if (i == L::bPFull || i == L::bPFull + 1) cnt = kGroupThreads;
-      if (i == L::bXch || i == L::bXch + 1 || i == L::bOFree) cnt = kSoftmaxThreads;
+      if (i == L::bInfoEmpty || i == L::bInfoEmpty + 1) cnt = 2 + kSoftmaxThreads;
+      if (i >= L::bPFull && i < L::bPFull + kSBuf) cnt = kSoftmaxThreads;
+      if (i == L::bOFree) cnt = kSoftmaxThreads;
       mbar_init(bar(i), cnt);
     }
     *abort_flag = 0;
@@ -351,12 +364,14 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   } else if (warp == kProducerWarp) {
     regs_dec<kControlRegs>();
     // ------------------------------------------------------------- producer
-    // Lane 0 streams Q and K, lane 1 streams V, each as far ahead as its
-    // ring allows. Each lane waits for all of its own copies to land before
-    // it leaves, so no copy can outlive the CTA's shared memory.
+    // Lane 0 loads each tile's Q, and K and V^T tiles through the ring in the
+    // order the MMA warp consumes them: K(0), K(1), then K(j+2) and V(j) for
+    // each step j (2 * n_steps items per tile). A stage is refilled once the
+    // MMAs that read it are done. The lane waits for all of its own copies to
+    // land before it leaves, so no copy can outlive the CTA's shared memory.
     if (lane == 0) {
-      int issued[KST] = {0};
-      int q_loads = 0, kcnt = 0;
+      int issued[KVST] = {0};
+      int q_loads = 0, c = 0;
       for (int it = 0;; ++it) {
         const int x = it & 1;
         if (!mbar_wait(bar(L::bInfoFull + x), (it >> 1) & 1, abort_sig)) { fail(kSiteInfo); break; }
@@ -364,6 +379,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const int n = hd[3];
         if (n < 0) break;
         const int b = hd[0], h = hd[1], qb0 = 2 * hd[2];
+        const int bh = b * a.H + h;
         const uint16_t* inf = info + x * kMaxNbAttn;
         // the previous tile's QKs are done with the Q buffer
         if (it >= 1 && !mbar_wait(bar(L::bQEmpty), (it - 1) & 1, abort_sig)) { fail(kSiteQFull); break; }
@@ -375,83 +391,62 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         dh * 64, (qb0 + qh) * kBlock, h, b);
         const int n_steps = (n + 1) >> 1;
         bool ok = true;
-        for (int j = 0; j < n_steps; ++j, ++kcnt) {
-          const int nblk = (2 * j + 1 < n) ? 2 : 1;
-          const int ks = kcnt % KST;
-          if (kcnt >= KST && !mbar_wait(bar(L::bKEmpty + ks), ((kcnt / KST) - 1) & 1, abort_sig)) {
-            fail(kSiteKStage);
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(bar(L::bKFull + ks), nblk * kBlock * D * 2);
-          ++issued[ks];
-          for (int kh = 0; kh < nblk; ++kh) {
-            const int jk = inf[2 * j + kh] >> 2;
-            for (int dh = 0; dh < D / 64; ++dh)
-              tma_load_4d(sbase + L::kK + ks * L::kKBytes + dh * L::kRegion + kh * 8192, &tm_k,
-                          bar(L::bKFull + ks), dh * 64, jk * kBlock, h, b);
+        for (int t = 0; t < n_steps + 2 && ok; ++t) {
+          for (int kind = 0; kind < 2; ++kind) {       // 0: K(t), 1: V(t - 2)
+            const int js = kind == 0 ? t : t - 2;
+            if (js < 0 || js >= n_steps) continue;
+            const int st = c % KVST;
+            if (c >= KVST &&
+                !mbar_wait(bar(L::bKVEmpty + st), ((c / KVST) - 1) & 1, abort_sig)) {
+              fail(kSiteKVStage);
+              ok = false;
+              break;
+            }
+            const int nblk = (2 * js + 1 < n) ? 2 : 1;
+            mbar_arrive_expect_tx(bar(L::bKVFull + st), nblk * kBlock * D * 2);
+            ++issued[st];
+            const uint32_t dst = sbase + L::kKV + st * L::kStageBytes;
+            for (int kh = 0; kh < nblk; ++kh) {
+              const int jk = inf[2 * js + kh] >> 2;
+              if (kind == 0) {
+                for (int dh = 0; dh < D / 64; ++dh)
+                  tma_load_4d(dst + dh * L::kRegion + kh * 8192, &tm_k, bar(L::bKVFull + st),
+                              dh * 64, jk * kBlock, h, b);
+              } else {
+                tma_load_3d(dst + kh * L::kVHalf, &tm_vt, bar(L::bKVFull + st), jk * kBlock, 0, bh);
+              }
+            }
+            ++c;
           }
         }
         if (!ok) break;
         mbar_arrive(bar(L::bInfoEmpty + x));
       }
       if (q_loads) mbar_wait(bar(L::bQFull), (q_loads - 1) & 1, drain_sig);
-      for (int s2 = 0; s2 < KST; ++s2)
-        if (issued[s2]) mbar_wait(bar(L::bKFull + s2), (issued[s2] - 1) & 1, drain_sig);
-    } else if (lane == 1) {
-      int issued[VST] = {0};
-      int vcnt = 0;
-      for (int it = 0;; ++it) {
-        const int x = it & 1;
-        if (!mbar_wait(bar(L::bInfoFull + x), (it >> 1) & 1, abort_sig)) { fail(kSiteInfo); break; }
-        const volatile int* hd = hdr + 4 * x;
-        const int n = hd[3];
-        if (n < 0) break;
-        const int bh = hd[0] * a.H + hd[1];
-        const uint16_t* inf = info + x * kMaxNbAttn;
-        const int n_steps = (n + 1) >> 1;
-        bool ok = true;
-        for (int j = 0; j < n_steps; ++j, ++vcnt) {
-          const int nblk = (2 * j + 1 < n) ? 2 : 1;
-          const int vs = vcnt % VST;
-          if (vcnt >= VST && !mbar_wait(bar(L::bVEmpty + vs), ((vcnt / VST) - 1) & 1, abort_sig)) {
-            fail(kSiteVStage);
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(bar(L::bVFull + vs), nblk * kBlock * D * 2);
-          ++issued[vs];
-          for (int kh = 0; kh < nblk; ++kh) {
-            const int jk = inf[2 * j + kh] >> 2;
-            tma_load_3d(sbase + L::kV + vs * L::kVBytes + kh * L::kVHalf, &tm_vt,
-                        bar(L::bVFull + vs), jk * kBlock, 0, bh);
-          }
-        }
-        if (!ok) break;
-        mbar_arrive(bar(L::bInfoEmpty + x));
-      }
-      for (int s2 = 0; s2 < VST; ++s2)
-        if (issued[s2]) mbar_wait(bar(L::bVFull + s2), (issued[s2] - 1) & 1, drain_sig);
+      for (int s2 = 0; s2 < KVST; ++s2)
+        if (issued[s2]) mbar_wait(bar(L::bKVFull + s2), (issued[s2] - 1) & 1, drain_sig);
     }
   } else if (warp == kMmaWarp) {
     regs_dec<kControlRegs>();
     // ------------------------------------------------------------------ MMA
     // The whole warp runs this loop in step (warp-uniform waits); elect.sync
-    // picks the lane that issues each batch of MMAs and each commit.
+    // picks the lane that issues each batch of MMAs and each commit. Order per
+    // tile: QK(0), QK(1), then for each step j: QK(j+2) (if any), PV(j) --
+    // the same order in which the producer fills the ring.
     constexpr uint32_t kIdQK128 = idesc_f16(BM, 128, 1);
     constexpr uint32_t kIdQK64 = idesc_f16(BM, 64, 1);
     constexpr uint32_t kIdPV = idesc_f16(BM, D, 0);
     // Descriptors: Q's K slices (start address stepped by 32 bytes inside a
     // 128-byte swizzle row, then by one 16 KB region per 64 elements), and
-    // the K/V stage bases.
+    // the ring's base.
     uint64_t qd[D / 16];
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk)
       qd[kk] = sdesc_kmajor_sw128(sbase + L::kQ + (kk >> 2) * L::kRegion + (kk & 3) * 32);
-    const uint64_t k0 = sdesc_kmajor_sw128(sbase + L::kK);
-    const uint64_t v0 = sdesc_kmajor_sw128(sbase + L::kV);
-    int kcnt = 0, vcnt = 0;
-    int grp_steps0 = 0, grp_steps1 = 0;  // steps of each group in earlier tiles
+    const uint64_t kv0 = sdesc_kmajor_sw128(sbase + L::kKV);
+    const uint32_t o_tmem = tmem + kColO;
+    int c = 0;        // ring items consumed so far
+    int gs0 = 0;      // global index (over this CTA's tiles) of the tile's first step
     bool ok = true;
     for (int it = 0; ok; ++it) {
       const int x = it & 1;
@@ -467,71 +462,72 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         break;
       }
       tc_fence_after();
+      // QK(j) into S[(gs0 + j) % 3]. That buffer last held step gs0 + j - 3,
+      // whose PV -- the last reader of its P -- this warp issued earlier; the
+      // tensor pipe runs the MMAs in order.
       auto issue_qk = [&](int j) -> bool {
-        const int ks = kcnt % KST;
-        if (!mbar_wait_warp(bar(L::bKFull + ks), (kcnt / KST) & 1, abort_sig)) {
-          if (lane == 0) fail(kSiteKFull);
+        const int st = c % KVST;
+        if (!mbar_wait_warp(bar(L::bKVFull + st), (c / KVST) & 1, abort_sig)) {
+          if (lane == 0) fail(kSiteKVFull);
           return false;
         }
         tc_fence_after();
+        const int b = (gs0 + j) % kSBuf;
         const uint32_t idesc = (2 * j + 1 < n) ? kIdQK128 : kIdQK64;
-        const uint32_t d_tmem = tmem + kColS + (j & 1) * 128;
-        const uint64_t kb = k0 + static_cast<uint64_t>(ks * (L::kKBytes >> 4));
+        const uint32_t d_tmem = tmem + kColS + b * 128;
+        const uint64_t kb = kv0 + static_cast<uint64_t>(st * (L::kStageBytes >> 4));
         uint64_t kd[D / 16];
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
           kd[kk] = kb + static_cast<uint64_t>(((kk >> 2) * L::kRegion + (kk & 3) * 32) >> 4);
 #pragma unroll
-        for (int g = 0; g < D / 64; ++g)
-          umma_ss_x4_elect(d_tmem, qd[4 * g], qd[4 * g + 1], qd[4 * g + 2], qd[4 * g + 3],
-                           kd[4 * g], kd[4 * g + 1], kd[4 * g + 2], kd[4 * g + 3], idesc, g > 0);
-        umma_commit_elect(bar(L::bSFull + (j & 1)));
-        umma_commit_elect(bar(L::bKEmpty + ks));
+        for (int h4 = 0; h4 < D / 64; ++h4)
+          umma_ss_x4_elect(d_tmem, qd[4 * h4], qd[4 * h4 + 1], qd[4 * h4 + 2], qd[4 * h4 + 3],
+                           kd[4 * h4], kd[4 * h4 + 1], kd[4 * h4 + 2], kd[4 * h4 + 3], idesc,
+                           h4 > 0);
+        umma_commit_elect(bar(L::bSFull + b));
+        umma_commit_elect(bar(L::bKVEmpty + st));
         if (j == n_steps - 1) umma_commit_elect(bar(L::bQEmpty));  // Q no longer read
-        ++kcnt;
+        ++c;
         return true;
       };
       if (n_steps == 0) umma_commit_elect(bar(L::bQEmpty));
       for (int j = 0; j < 2 && j < n_steps && ok; ++j) ok = issue_qk(j);
       if (!ok) break;
-      // the previous tile's epilogue has read both O accumulators
+      // the previous tile's epilogue has read O
       if (it >= 1 && !mbar_wait_warp(bar(L::bOFree), (it - 1) & 1, abort_sig)) {
         if (lane == 0) fail(kSiteOFree);
         break;
       }
       tc_fence_after();
       for (int j = 0; j < n_steps && ok; ++j) {
-        const int g = j & 1;
-        const int gstep = (g == 0 ? grp_steps0 : grp_steps1) + (j >> 1);
-        if (!mbar_wait_warp(bar(L::bPFull + g), gstep & 1, abort_sig)) {
+        // QK(j+2) needs no softmax result, so it goes first: the tensor pipe
+        // works on it while this warp waits for P(j).
+        if (j + 2 < n_steps && !issue_qk(j + 2)) {
+          ok = false;
+          break;
+        }
+        const int gsj = gs0 + j, b = gsj % kSBuf, st = c % KVST;
+        bool unused = false;
+        if (!mbar_wait2_warp(bar(L::bPFull + b), (gsj / kSBuf) & 1, bar(L::bKVFull + st),
+                             (c / KVST) & 1, false, 0u, 0u, &unused, abort_sig)) {
           if (lane == 0) fail(kSitePFull);
           ok = false;
           break;
         }
         tc_fence_after();
-        const int vs = vcnt % VST;
-        if (!mbar_wait_warp(bar(L::bVFull + vs), (vcnt / VST) & 1, abort_sig)) {
-          if (lane == 0) fail(kSiteVFull);
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t pa = tmem + kColS + g * 128;   // P(j) over S(j)
-        const uint32_t od = tmem + kColO + g * 128;   // this group's O
-        const uint64_t vb = v0 + static_cast<uint64_t>(vs * (L::kVBytes >> 4));
-        umma_ts_x4_elect(od, pa, vb, vb + 2, vb + 4, vb + 6, kIdPV, j >= 2);
+        const uint32_t pa = tmem + kColS + b * 128;    // P(j) over S(j)
+        const uint64_t vb = kv0 + static_cast<uint64_t>(st * (L::kStageBytes >> 4));
+        umma_ts_x4_elect(o_tmem, pa, vb, vb + 2, vb + 4, vb + 6, kIdPV, j > 0);
         if (2 * j + 1 < n) {
           const uint64_t vh = vb + (L::kVHalf >> 4);
-          umma_ts_x4_elect(od, pa + 32, vh, vh + 2, vh + 4, vh + 6, kIdPV, 1u);
+          umma_ts_x4_elect(o_tmem, pa + 32, vh, vh + 2, vh + 4, vh + 6, kIdPV, 1u);
         }
-        umma_commit_elect(bar(L::bVEmpty + vs));
-        ++vcnt;
-        // S[g] now belongs to QK(j+2): PV(j), the last reader of P(j), was
-        // issued just before, and the tensor pipe runs the MMAs in order.
-        if (j + 2 < n_steps && !issue_qk(j + 2)) ok = false;
+        umma_commit_elect(bar(L::bKVEmpty + st));
+        umma_commit_elect(bar(L::bPVDone));
+        ++c;
       }
-      grp_steps0 += (n_steps + 1) >> 1;
-      grp_steps1 += n_steps >> 1;
+      gs0 += n_steps;
       if (!ok) break;
       umma_commit_elect(bar(L::bTileDone));
       if (elect_one()) mbar_arrive(bar(L::bInfoEmpty + x));
@@ -544,25 +540,41 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   } else {
     regs_inc<kSoftmaxRegs>();
     // ------------------------------------------------------------- softmax
-    const int grp = warp >> 2;                 // 0: even steps, 1: odd steps
-    const int quarter = warp & 3;
+    const int quarter = warp & 3;              // TMEM lane quarter
+    const int half = warp >> 2;                // key block of the step this thread takes
     const int r = quarter * 32 + lane;         // tile row == TMEM lane
     const int qh = r >> 6;                     // query block of this row (warp-uniform)
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    const uint32_t s_col = kColS + grp * 128;
-    const uint32_t o_col = kColO + grp * 128;
+    const uint32_t o_col = kColO + half * (D / 2);   // this thread's half of O's columns
+    const uint32_t pair_bar = 1 + quarter;     // named barrier of warps quarter, quarter + 4
     const int last_valid = S - (Nb - 1) * kBlock;  // tokens in the last block
     const float cl2 = a.scale_log2;
-    float* xch = reinterpret_cast<float*>(smem + L::kXch);
-    int gstep = 0;                             // this group's steps so far (all tiles)
+    float* xv = reinterpret_cast<float*>(smem + L::kXch);       // [2 slots][2 halves][BM]
+    int* xs = reinterpret_cast<int*>(smem + L::kXch) + 2 * 2 * BM;
+    int xc = 0;                                // exchanges so far (slot xc & 1)
+    // Swap a value and a stop bit with the other thread of this row. Both
+    // warps of a pair pass the same sequence of exchanges, and a stop from
+    // either ends both, so neither is ever left waiting at the pair barrier.
+    // Slots alternate: a slot is rewritten only after the next exchange,
+    // which the partner reaches after reading it.
+    auto pair_xchg = [&](float v, bool stop, float& other) -> bool {
+      const int sl = xc & 1;
+      ++xc;
+      xv[(sl * 2 + half) * BM + r] = v;
+      xs[(sl * 2 + half) * BM + r] = stop ? 1 : 0;
+      named_bar_sync(pair_bar, 64);
+      other = xv[(sl * 2 + (half ^ 1)) * BM + r];
+      return stop || xs[(sl * 2 + (half ^ 1)) * BM + r] != 0;
+    };
+    int gs = 0;                                // this CTA's steps so far (all tiles)
     bool ok = true;
 
     for (int it = 0; ok; ++it) {
       const int x = it & 1;
-      if (!mbar_wait_warp(bar(L::bInfoFull + x), (it >> 1) & 1, abort_sig)) {
-        if (lane == 0) fail(kSiteInfo);
-        break;
-      }
+      bool stop = !mbar_wait_warp(bar(L::bInfoFull + x), (it >> 1) & 1, abort_sig);
+      if (stop && lane == 0) fail(kSiteInfo);
+      float unused;
+      if (pair_xchg(0.f, stop, unused)) break;
       const volatile int* hd = hdr + 4 * x;
       const int n = hd[3];
       if (n < 0) break;
@@ -572,125 +584,91 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       const int t = qb0 * kBlock + r;          // query token
       float m_run = -INFINITY, l_run = 0.f;
 
-      for (int j = grp; j < n_steps; j += 2, ++gstep) {
-        if (!mbar_wait_warp(bar(L::bSFull + grp), gstep & 1, abort_sig)) {
-          if (lane == 0) fail(kSiteSFull);
+      for (int j = 0; j < n_steps; ++j, ++gs) {
+        const int sb = gs % kSBuf;
+        const uint32_t s_col = kColS + sb * 128;
+        stop = !mbar_wait_warp(bar(L::bSFull + sb), (gs / kSBuf) & 1, abort_sig);
+        if (stop && lane == 0) fail(kSiteSFull);
+        tc_fence_after();
+        const bool has = half == 0 || 2 * j + 1 < n;   // an odd walk's last step has one block
+        const uint32_t e = has ? inf[2 * j + half] : 0u;
+        const bool mem = has && ((e >> qh) & 1u);
+        uint32_t sr[64];
+        float mx = -INFINITY;
+        if (mem && !stop) {
+          tmem_ld32(lane_base + s_col + half * 64, sr);
+          tmem_ld32(lane_base + s_col + half * 64 + 32, sr + 32);
+          tmem_wait_ld();
+          mask_tail(sr, e, Nb, last_valid);
+          mx = max64(sr);
+        }
+        float mo;
+        if (pair_xchg(mx, stop, mo)) {
           ok = false;
           break;
         }
-        tc_fence_after();
-        const int nblk = (2 * j + 1 < n) ? 2 : 1;
-        const uint32_t e0 = inf[2 * j];
-        const uint32_t e1 = nblk == 2 ? inf[2 * j + 1] : 0u;
-        const bool mem0 = (e0 >> qh) & 1u;
-        const bool mem1 = nblk == 2 && ((e1 >> qh) & 1u);
-        uint32_t sr[BN];
-        if (mem0) {
-          tmem_ld32(lane_base + s_col, sr);
-          tmem_ld32(lane_base + s_col + 32, sr + 32);
-        }
-        if (mem1) {
-          tmem_ld32(lane_base + s_col + 64, sr + 64);
-          tmem_ld32(lane_base + s_col + 96, sr + 96);
-        }
-        tmem_wait_ld();
-        // the ragged last block: keys past S weigh exactly zero
-        if (mem0 && static_cast<int>(e0 >> 2) == Nb - 1) {
-#pragma unroll
-          for (int u = 0; u < 64; ++u)
-            if (u >= last_valid) sr[u] = __float_as_uint(-INFINITY);
-        }
-        if (mem1 && static_cast<int>(e1 >> 2) == Nb - 1) {
-#pragma unroll
-          for (int u = 0; u < 64; ++u)
-            if (u >= last_valid) sr[64 + u] = __float_as_uint(-INFINITY);
-        }
-        float mx = -INFINITY;
-        if (mem0) mx = fmaxf(mx, max64(sr));
-        if (mem1) mx = fmaxf(mx, max64(sr + 64));
-        const float bmax = mx * cl2;           // the scale is positive: max commutes
+        const float bmax = fmaxf(mx, mo) * cl2;  // the scale is positive: max commutes
         float m_new = m_run;
         if (bmax > m_run + kRescaleLog2) m_new = bmax;  // also the first finite block
         const bool rescale = (m_new != m_run) && (m_run != -INFINITY);
-        const float alpha = (m_new == m_run) ? 1.f : fast_exp2(m_run - m_new);
-        const float negm = -m_new;
-        // P(j) over the consumed S(j) columns: keys 0-63 -> columns 0-31,
-        // keys 64-127 -> columns 32-63 (two fp16 per column); each half is
-        // stored as soon as it is ready.
+        const float alpha = rescale ? fast_exp2(m_run - m_new) : 1.f;
+        // P over this thread's 64 keys: 32 columns (two fp16 per column) at
+        // the start of its half of the consumed S columns.
         float rs = 0.f;
-        {
+        if (has) {
           uint32_t pk[32];
-          if (mem0) rs += exp_pack64(sr, cl2, negm, pk);
+          if (mem) rs = exp_pack64(sr, cl2, -m_new, pk);
           else {
 #pragma unroll
             for (int u = 0; u < 32; ++u) pk[u] = 0u;
           }
-          tmem_st32(lane_base + s_col, pk);
-        }
-        if (nblk == 2) {
-          uint32_t pk[32];
-          if (mem1) rs += exp_pack64(sr + 64, cl2, negm, pk);
-          else {
-#pragma unroll
-            for (int u = 0; u < 32; ++u) pk[u] = 0u;
-          }
-          tmem_st32(lane_base + s_col + 32, pk);
+          tmem_st32(lane_base + s_col + half * 32, pk);
         }
         l_run = l_run * alpha + rs;
         m_run = m_new;
-        if (__any_sync(0xffffffffu, rescale)) {
-          // S(j) ready means QK(j) is done, and QK(j) was issued after this
-          // group's previous PV(j-2): that PV is done too, and PV(j) waits for
-          // p_full(j), so O[grp] is stable here without another wait.
-  #pragma unroll 1
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t o[32];
-            tmem_ld32(lane_base + o_col + 32 * c, o);
-            tmem_wait_ld();
+        if (__any_sync(full, rescale)) {
+          // O holds this tile's PVs of the steps before j; the last of them
+          // must be done before O is rescaled (PV(j) waits for this step's
+          // p_full, so no later PV can be running).
+          if (!mbar_wait_warp(bar(L::bPVDone), (gs - 1) & 1, abort_sig)) {
+            if (lane == 0) fail(kSitePVDone);
+          } else {
+            tc_fence_after();
+#pragma unroll 1
+            for (int cc = 0; cc < D / 64; ++cc) {
+              uint32_t o[32];
+              tmem_ld32(lane_base + o_col + 32 * cc, o);
+              tmem_wait_ld();
 #pragma unroll
-            for (int u = 0; u < 32; ++u) o[u] = __float_as_uint(__uint_as_float(o[u]) * alpha);
-            tmem_st32(lane_base + o_col + 32 * c, o);
+              for (int u = 0; u < 32; ++u) o[u] = __float_as_uint(__uint_as_float(o[u]) * alpha);
+              tmem_st32(lane_base + o_col + 32 * cc, o);
+            }
           }
         }
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(bar(L::bPFull + grp));
+        mbar_arrive(bar(L::bPFull + sb));
       }
       if (!ok) break;
       mbar_arrive(bar(L::bInfoEmpty + x));     // done with this walk
 
       // -------------------------------------------------------- epilogue
-      // Merge the two groups' partial results for this row: both threads of
-      // the row (same lane, groups 0 and 1) post (m, l), then each writes
-      // half of the output columns.
-      float* xs = xch + x * (2 * 2 * BM);
-      xs[(grp * 2 + 0) * BM + r] = m_run;
-      xs[(grp * 2 + 1) * BM + r] = l_run;
-      mbar_arrive(bar(L::bXch + x));
-      if (!mbar_wait_warp(bar(L::bXch + x), (it >> 1) & 1, abort_sig) ||
-          !mbar_wait_warp(bar(L::bTileDone), it & 1, abort_sig)) {
-        if (lane == 0) fail(kSiteFin);
-        ok = false;
-        break;
-      }
+      // Both threads of the row add their partial sums; each writes its half
+      // of the output columns once every PV of the tile is done.
+      stop = !mbar_wait_warp(bar(L::bTileDone), it & 1, abort_sig);
+      if (stop && lane == 0) fail(kSiteFin);
+      float l_other;
+      if (pair_xchg(l_run, stop, l_other)) break;
       tc_fence_after();
-      const float m0 = xs[0 * BM + r], l0 = xs[1 * BM + r];
-      const float m1 = xs[2 * BM + r], l1 = xs[3 * BM + r];
-      const float m = fmaxf(m0, m1);
-      const float s0 = l0 > 0.f ? fast_exp2(m0 - m) : 0.f;   // group 0's weight
-      const float s1 = l1 > 0.f ? fast_exp2(m1 - m) : 0.f;   // group 1's weight
-      const float l_tot = l0 * s0 + l1 * s1;
+      const float l_tot = l_run + l_other;
       const float inv_l = l_tot > 0.f ? 1.f / l_tot : 0.f;
-      const float w0 = s0 * inv_l, w1 = s1 * inv_l;
       const bool row_ok = t < S;
       uint16_t* orow = a.o + b * a.os[0] + static_cast<int64_t>(t) * a.os[1] + h * a.os[2] +
-                       grp * (D / 2);
+                       half * (D / 2);
 #pragma unroll
-      for (int c = 0; c < D / 64; ++c) {
-        const uint32_t col = grp * (D / 2) + 32 * c;
-        uint32_t oa[32], ob[32];
-        tmem_ld32(lane_base + kColO + col, oa);
-        tmem_ld32(lane_base + kColO + 128 + col, ob);
+      for (int cc = 0; cc < D / 64; ++cc) {
+        uint32_t ov[32];
+        tmem_ld32(lane_base + o_col + 32 * cc, ov);
         tmem_wait_ld();
         if (row_ok) {
 #pragma unroll
@@ -698,25 +676,23 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             float f[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
-              // a group with no weight may not have written its O in this
-              // tile: select, never multiply, so stale TMEM cannot leak in
-              const float xa = s0 > 0.f ? __uint_as_float(oa[8 * v + u]) * w0 : 0.f;
-              const float xb = s1 > 0.f ? __uint_as_float(ob[8 * v + u]) * w1 : 0.f;
-              f[u] = xa + xb;
+              // a row without weight may face an O this tile never wrote:
+              // select, never multiply, so stale TMEM cannot leak in
+              f[u] = l_tot > 0.f ? __uint_as_float(ov[8 * v + u]) * inv_l : 0.f;
             }
             uint4 wv;
             wv.x = pack_bf162(f[0], f[1]);
             wv.y = pack_bf162(f[2], f[3]);
             wv.z = pack_bf162(f[4], f[5]);
             wv.w = pack_bf162(f[6], f[7]);
-            *reinterpret_cast<uint4*>(orow + 32 * c + 8 * v) = wv;
+            *reinterpret_cast<uint4*>(orow + 32 * cc + 8 * v) = wv;
           }
         }
       }
       tc_fence_before();
-      mbar_arrive(bar(L::bOFree));             // both O accumulators read
-      if (row_ok && grp == 0 && a.lse) {
-        const float lse = l_tot > 0.f ? m * 0.69314718055994531f + logf(l_tot) : -INFINITY;
+      mbar_arrive(bar(L::bOFree));             // O read
+      if (row_ok && half == 0 && a.lse) {
+        const float lse = l_tot > 0.f ? m_run * 0.69314718055994531f + logf(l_tot) : -INFINITY;
         a.lse[(static_cast<int64_t>(b) * a.H + h) * S + t] = lse;
       }
     }

@@ -64,6 +64,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test of whether the phase of `parity` has completed.
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.b32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+  return ok != 0;
+}
+
 // One thread waits for the phase of `parity` to complete. Returns false if
 // the wait ran out of time or another role set *abort.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, AbortSignal abort) {
@@ -89,6 +100,36 @@ __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity,
   for (uint32_t it = 1;; ++it) {
     if (__all_sync(full, mbar_try_wait(bar, parity))) return true;
     if ((it & 63u) == 0u) {
+      int give_up = 0;
+      if ((threadIdx.x & 31) == 0)
+        give_up = abort.raised() || (globaltimer() - t0 > kWaitTimeoutNs);
+      if (__shfl_sync(full, give_up, 0)) return false;
+    }
+  }
+}
+
+// A converged warp waits until barriers a and b have both completed the given
+// phases. When has_c is set it also tests barrier c on every round and
+// reports in *c_done whether c's phase had completed by the round that
+// ended the wait. The tests of one round are independent, so their
+// latencies overlap: one round costs about one barrier round trip, where
+// waiting for a, b and c one after another costs three. Returns false on
+// timeout or abort, like mbar_wait_warp.
+__device__ __forceinline__ bool mbar_wait2_warp(uint32_t a, uint32_t pa, uint32_t b, uint32_t pb,
+                                                bool has_c, uint32_t c, uint32_t pc,
+                                                bool* c_done, AbortSignal abort) {
+  const unsigned full = 0xffffffffu;
+  unsigned long long t0 = 0;
+  for (uint32_t it = 0;; ++it) {
+    const bool ra = mbar_test(a, pa);
+    const bool rb = mbar_test(b, pb);
+    const bool rc = has_c && mbar_test(c, pc);
+    if (__all_sync(full, ra && rb)) {
+      *c_done = __all_sync(full, rc);
+      return true;
+    }
+    if (it == 0 && (threadIdx.x & 31) == 0) t0 = globaltimer();
+    if ((it & 63u) == 63u) {
       int give_up = 0;
       if ((threadIdx.x & 31) == 0)
         give_up = abort.raised() || (globaltimer() - t0 > kWaitTimeoutNs);

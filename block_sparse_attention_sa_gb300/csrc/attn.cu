@@ -98,8 +98,9 @@ struct Smem {
   static constexpr int bKVEmpty = bKVFull + KVST;     // [KVST] its MMAs are done with a stage
   static constexpr int bSFull = bKVEmpty + KVST;      // [kSBuf] QK into S[b] done
   static constexpr int bPFull = bSFull + kSBuf;       // [kSBuf] softmax wrote P over S[b]
-  static constexpr int bPVDone = bPFull + kSBuf;      // one phase per PV: that PV is done
-  static constexpr int bTileDone = bPVDone + 1;       // every PV of the tile done
+  static constexpr int bPVDone = bPFull + kSBuf;      // [2] PV number g (this CTA's count)
+                                                      // completes a phase of bPVDone + g % 2
+  static constexpr int bTileDone = bPVDone + 2;       // every PV of the tile done
   static constexpr int bOFree = bTileDone + 1;        // the epilogue has read O
   static constexpr int bFin = bOFree + 1;             // every MMA done (exit)
   static constexpr int kNumBars = bFin + 1;
@@ -280,18 +281,29 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         if (lane == 0) mbar_arrive(bar(L::bInfoFull + x));
         break;
       }
-      const int pair = tile % a.n_pairs;
+      const int slot = tile % a.n_pairs;
       const int bh = tile / a.n_pairs;
       const int h = bh % a.H, b = bh / a.H;
-      const int qb0 = 2 * pair;
-      const bool has_qb1 = qb0 + 1 < Nb;
+      // the tile's two query blocks qb0 < qb1 (qb1 = -1: qb0 alone)
+      int qb0 = 2 * slot, qb1 = qb0 + 1 < Nb ? qb0 + 1 : -1;
+      int bad = 0;
+      if (a.pairs) {
+        const uint32_t pe = a.pairs[static_cast<int64_t>(bh) * a.n_pairs + slot];
+        qb0 = static_cast<int>(pe & 0xffffu);
+        qb1 = (pe >> 16) == 0xffffu ? -1 : static_cast<int>(pe >> 16);
+        if (qb0 >= Nb || qb1 >= Nb || qb1 == qb0) {   // never written by the pairing kernels
+          bad = 1;
+          qb0 = 0;
+          qb1 = -1;
+        }
+      }
+      const bool has_qb1 = qb1 >= 0;
       // Union of the two query blocks' key lists with a 2-bit membership mask
       // per key block (bit 0: block 2p lists it, bit 1: block 2p+1 does),
       // ascending but rotated to start at the tile's own diagonal block: the
       // row maxima usually sit near the diagonal, so taking it first keeps
       // later steps from raising the running max (each raise rescales O).
       const int words = (Nb + 31) >> 5;
-      int bad = 0;
       if (a.row_ptr == nullptr) {
         const uint16_t m = has_qb1 ? 3 : 1;
         for (int j = lane; j < Nb; j += 32)
@@ -302,7 +314,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         __syncwarp();
         for (int half = 0; half < 2; ++half) {
           if (half == 1 && !has_qb1) break;
-          const int64_t r = (static_cast<int64_t>(b) * a.H + h) * Nb + qb0 + half;
+          const int64_t r = (static_cast<int64_t>(b) * a.H + h) * Nb + (half ? qb1 : qb0);
           const int beg = a.row_ptr[r], end = a.row_ptr[r + 1];
           if (beg < 0 || end < beg || end - beg > Nb) { bad = 1; continue; }
           uint32_t* bm = half ? bmB : bmA;
@@ -356,7 +368,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       if (lane == 0) {
         hd[0] = b;
         hd[1] = h;
-        hd[2] = pair;
+        hd[2] = static_cast<int>(static_cast<uint32_t>(qb0) | (static_cast<uint32_t>(qb1 & 0xffff) << 16));
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(L::bInfoFull + x));
@@ -378,7 +390,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const volatile int* hd = hdr + 4 * x;
         const int n = hd[3];
         if (n < 0) break;
-        const int b = hd[0], h = hd[1], qb0 = 2 * hd[2];
+        const int b = hd[0], h = hd[1];
+        // query rows of the two blocks; a missing second block reads zeros
+        const uint32_t pr = static_cast<uint32_t>(hd[2]);
+        const int qrow0 = static_cast<int>(pr & 0xffffu) * kBlock;
+        const int qrow1 = (pr >> 16) == 0xffffu ? Nb * kBlock : static_cast<int>(pr >> 16) * kBlock;
         const int bh = b * a.H + h;
         const uint16_t* inf = info + x * kMaxNbAttn;
         // the previous tile's QKs are done with the Q buffer
@@ -388,7 +404,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         for (int qh = 0; qh < 2; ++qh)
           for (int dh = 0; dh < D / 64; ++dh)
             tma_load_4d(sbase + L::kQ + dh * L::kRegion + qh * 8192, &tm_q, bar(L::bQFull),
-                        dh * 64, (qb0 + qh) * kBlock, h, b);
+                        dh * 64, qh ? qrow1 : qrow0, h, b);
         const int n_steps = (n + 1) >> 1;
         bool ok = true;
         for (int t = 0; t < n_steps + 2 && ok; ++t) {
@@ -524,7 +540,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           umma_ts_x4_elect(o_tmem, pa + 32, vh, vh + 2, vh + 4, vh + 6, kIdPV, 1u);
         }
         umma_commit_elect(bar(L::bKVEmpty + st));
-        umma_commit_elect(bar(L::bPVDone));
+        umma_commit_elect(bar(L::bPVDone + (gsj & 1)));
         ++c;
       }
       gs0 += n_steps;
@@ -578,10 +594,13 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       const volatile int* hd = hdr + 4 * x;
       const int n = hd[3];
       if (n < 0) break;
-      const int b = hd[0], h = hd[1], qb0 = 2 * hd[2];
+      const int b = hd[0], h = hd[1];
+      const uint32_t pr = static_cast<uint32_t>(hd[2]);
+      const int qb = qh ? ((pr >> 16) == 0xffffu ? -1 : static_cast<int>(pr >> 16))
+                        : static_cast<int>(pr & 0xffffu);
       const uint16_t* inf = info + x * kMaxNbAttn;
       const int n_steps = (n + 1) >> 1;
-      const int t = qb0 * kBlock + r;          // query token
+      const int t = qb * kBlock + (r & (kBlock - 1));   // query token (< 0: no block)
       float m_run = -INFINITY, l_run = 0.f;
 
       for (int j = 0; j < n_steps; ++j, ++gs) {
@@ -627,10 +646,13 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         l_run = l_run * alpha + rs;
         m_run = m_new;
         if (__any_sync(full, rescale)) {
-          // O holds this tile's PVs of the steps before j; the last of them
-          // must be done before O is rescaled (PV(j) waits for this step's
-          // p_full, so no later PV can be running).
-          if (!mbar_wait_warp(bar(L::bPVDone), (gs - 1) & 1, abort_sig)) {
+          // O holds this tile's PVs of the steps before j; the last of them,
+          // PV number gs - 1, must be done before O is rescaled (PV(j) waits
+          // for this step's p_full, so no later PV can be running). A parity
+          // wait needs the barrier within one phase of the one waited for:
+          // S(j) is written after PV(gs - 3) in the tensor pipe's order, so
+          // on the barrier of gs - 1's parity the phase before it is done.
+          if (!mbar_wait_warp(bar(L::bPVDone + ((gs - 1) & 1)), ((gs - 1) >> 1) & 1, abort_sig)) {
             if (lane == 0) fail(kSitePVDone);
           } else {
             tc_fence_after();
@@ -662,7 +684,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       tc_fence_after();
       const float l_tot = l_run + l_other;
       const float inv_l = l_tot > 0.f ? 1.f / l_tot : 0.f;
-      const bool row_ok = t < S;
+      const bool row_ok = qb >= 0 && t < S;
       uint16_t* orow = a.o + b * a.os[0] + static_cast<int64_t>(t) * a.os[1] + h * a.os[2] +
                        half * (D / 2);
 #pragma unroll
@@ -704,47 +726,47 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
 }
 
-// V [B,S,H,D] bf16 -> vt [B*H][D][s_pad] fp16. grid (ceil(S/64), H, B), 256 threads.
+// V [B,S,H,D] bf16 -> vt [B*H][D][s_pad] fp16 (key-contiguous). Each thread
+// converts an 8-token x 8-d block: eight 16-byte loads (one token row each,
+// the D/8 threads of a token group read whole rows), a transpose in
+// registers, eight 16-byte stores (one d row each). Tokens in [S, s_pad)
+// are written as zeros. grid (ceil(s_pad / tokens per CTA), H, B), 256 threads.
 template <int D>
 __global__ void __launch_bounds__(256)
 pack_v_kernel(const uint16_t* __restrict__ v, int64_t vs0, int64_t vs1, int64_t vs2, int S, int H,
               int s_pad, uint16_t* __restrict__ vt, int32_t* dev_status) {
-  __shared__ uint16_t tile[kBlock][D + 8];
-  const int s0 = blockIdx.x * kBlock, h = blockIdx.y, b = blockIdx.z;
+  constexpr int kChunks = D / 8;                     // threads per token group
+  constexpr int kTokens = 256 / kChunks * 8;         // tokens per CTA
+  const int c = threadIdx.x % kChunks, g = threadIdx.x / kChunks;
+  const int h = blockIdx.y, b = blockIdx.z;
+  const int t0 = blockIdx.x * kTokens + g * 8;
   bool range = false;
-  constexpr int VPR = D / 8;  // 16-byte vectors per token row
-  for (int idx = threadIdx.x; idx < kBlock * VPR; idx += 256) {
-    const int r = idx / VPR, c = (idx % VPR) * 8;
-    uint4 w = make_uint4(0, 0, 0, 0);
-    if (s0 + r < S)
-      w = __ldg(reinterpret_cast<const uint4*>(v + b * vs0 + static_cast<int64_t>(s0 + r) * vs1 +
-                                               h * vs2 + c));
-    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+  if (t0 < s_pad) {
+    uint4 w[8];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const float f = __uint_as_float((hh ? (ww[u] & 0xffff0000u) : (ww[u] << 16)));
-        const __half hv = __float2half_rn(f);
-        if (isinf(__half2float(hv)) && !isinf(f)) range = true;
-        tile[r][c + 2 * u + hh] = *reinterpret_cast<const uint16_t*>(&hv);
-      }
+    for (int q = 0; q < 8; ++q) {
+      w[q] = make_uint4(0u, 0u, 0u, 0u);
+      if (t0 + q < S)
+        w[q] = __ldg(reinterpret_cast<const uint4*>(v + b * vs0 + static_cast<int64_t>(t0 + q) * vs1 +
+                                                    h * vs2 + 8 * c));
     }
-  }
-  __syncthreads();
-  uint16_t* dst = vt + (static_cast<int64_t>(b) * H + h) * D * s_pad;
-  for (int idx = threadIdx.x; idx < D * (kBlock / 8); idx += 256) {
-    const int d = idx / (kBlock / 8), c = (idx % (kBlock / 8)) * 8;
-    if (s0 + c >= s_pad) continue;
-    uint16_t e[8];
+    uint16_t* dst = vt + (static_cast<int64_t>(b) * H + h) * D * s_pad + static_cast<int64_t>(8 * c) * s_pad + t0;
 #pragma unroll
-    for (int u = 0; u < 8; ++u) e[u] = tile[c + u][d];
-    uint4 w;
-    w.x = e[0] | (static_cast<uint32_t>(e[1]) << 16);
-    w.y = e[2] | (static_cast<uint32_t>(e[3]) << 16);
-    w.z = e[4] | (static_cast<uint32_t>(e[5]) << 16);
-    w.w = e[6] | (static_cast<uint32_t>(e[7]) << 16);
-    *reinterpret_cast<uint4*>(dst + static_cast<int64_t>(d) * s_pad + s0 + c) = w;
+    for (int p = 0; p < 8; ++p) {
+      float f[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const uint32_t word = (&w[q].x)[p >> 1];
+        f[q] = __uint_as_float((p & 1) ? (word & 0xffff0000u) : (word << 16));
+        range |= fabsf(f[q]) > 65504.f && !isinf(f[q]);
+      }
+      uint4 o;
+      o.x = pack_half2(f[0], f[1]);
+      o.y = pack_half2(f[2], f[3]);
+      o.z = pack_half2(f[4], f[5]);
+      o.w = pack_half2(f[6], f[7]);
+      *reinterpret_cast<uint4*>(dst + static_cast<int64_t>(p) * s_pad) = o;
+    }
   }
   if (__syncthreads_or(range) && threadIdx.x == 0) set_status(dev_status, SA_DEV_RANGE);
 }
@@ -768,7 +790,8 @@ cudaError_t launch_attn_d(const AttnMaps& m, const AttnArgs& a, cudaStream_t st)
 
 cudaError_t launch_pack_v(const uint16_t* v, const int64_t vs[3], int B, int S, int H, int D,
                           int s_pad, uint16_t* vt, int32_t* dev_status, cudaStream_t st) {
-  dim3 grid((S + kBlock - 1) / kBlock, H, B);
+  const int per_cta = 256 / (D / 8) * 8;
+  dim3 grid((s_pad + per_cta - 1) / per_cta, H, B);
   if (D == 128)
     pack_v_kernel<128><<<grid, 256, 0, st>>>(v, vs[0], vs[1], vs[2], S, H, s_pad, vt, dev_status);
   else

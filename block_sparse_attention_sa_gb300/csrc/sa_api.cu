@@ -98,10 +98,28 @@ size_t vt_bytes(const sa_params* p) {
   return static_cast<size_t>(p->B) * p->H * p->D * s_pad_of(p->S) * 2;
 }
 
-// V repacked to fp16, then (256-byte aligned) the persistent kernel's tile counter.
-size_t attn_ws_bytes(const sa_params* p) {
-  return ((vt_bytes(p) + 255) & ~static_cast<size_t>(255)) + 256;
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+// Attention workspace, each part 256-byte aligned: V repacked to fp16, the
+// persistent kernel's tile counter, the pairing's candidate lists and its
+// tile list (last).
+struct AttnLayout {
+  size_t vt, counter, cand, pairs, total;
+};
+
+AttnLayout attn_layout(const sa_params* p) {
+  const int Nb = num_blocks(p->S);
+  const int64_t bh = static_cast<int64_t>(p->B) * p->H;
+  AttnLayout L{};
+  L.vt = 0;
+  L.counter = align256(vt_bytes(p));
+  L.cand = L.counter + 256;
+  L.pairs = L.cand + align256(pair_cand_bytes(bh * Nb));
+  L.total = L.pairs + align256(static_cast<size_t>(bh) * ((Nb + 1) / 2) * sizeof(uint32_t));
+  return L;
 }
+
+size_t attn_ws_bytes(const sa_params* p) { return attn_layout(p).total; }
 
 sa_status attn_common(const sa_params* p, const void* q, const void* k, const void* v,
                       const int32_t* row_ptr, const int32_t* col_idx, void* o, float* lse,
@@ -130,9 +148,24 @@ sa_status attn_common(const sa_params* p, const void* q, const void* k, const vo
                                 p->D, s_pad_of(p->S), static_cast<uint16_t*>(ws), dev_status, st);
   if (e != cudaSuccess) return SA_ERR_CUDA;
 
+  const AttnLayout L = attn_layout(p);
+  char* wsb = static_cast<char*>(ws);
   AttnArgs a{};
   a.row_ptr = dense ? nullptr : row_ptr;
   a.col_idx = dense ? nullptr : col_idx;
+  a.pairs = nullptr;
+  if (!dense && Nb > 2) {
+    // choose the query-block pairs of the 128-row tiles from the route
+    PairArgs pa{};
+    pa.row_ptr = row_ptr;
+    pa.col_idx = col_idx;
+    pa.cand = reinterpret_cast<int16_t*>(wsb + L.cand);
+    pa.pairs = reinterpret_cast<uint32_t*>(wsb + L.pairs);
+    pa.Nb = Nb;
+    pa.n_pairs = (Nb + 1) / 2;
+    if (launch_pair(pa, p->B * p->H, st) != cudaSuccess) return SA_ERR_CUDA;
+    a.pairs = pa.pairs;
+  }
   a.o = static_cast<uint16_t*>(o);
   a.lse = lse;
   a.dev_status = dev_status;
@@ -144,8 +177,7 @@ sa_status attn_common(const sa_params* p, const void* q, const void* k, const vo
   a.n_pairs = (Nb + 1) / 2;
   a.scale_log2 = static_cast<float>(scale64_of(p) * 1.4426950408889634);
   a.n_tiles = p->B * p->H * a.n_pairs;
-  a.tile_counter = reinterpret_cast<int*>(static_cast<char*>(ws) +
-                                          ((vt_bytes(p) + 255) & ~static_cast<size_t>(255)));
+  a.tile_counter = reinterpret_cast<int*>(wsb + L.counter);
   if (cudaMemsetAsync(a.tile_counter, 0, sizeof(int), st) != cudaSuccess) return SA_ERR_CUDA;
   return from_cuda(launch_attn(p->D, maps, a, st));
 }

@@ -50,9 +50,25 @@ cudaError_t launch_route(const RouteArgs& a, cudaStream_t st);
 
 // ---------------------------------------------------------- attention ---
 
+// ---------------------------------------------------- tile pairing ---
+
+constexpr int kPairWindow = 32;     // query blocks pair only with blocks this close
+
+struct PairArgs {
+  const int32_t* row_ptr;  // the route (CSR)
+  const int32_t* col_idx;
+  int16_t* cand;           // [B*H*Nb][2 kPairWindow] candidates of each block, best first
+  uint32_t* pairs;         // [B*H][n_pairs] a | b << 16 (a < b; b = 0xffff: a alone)
+  int Nb, n_pairs;
+};
+
+size_t pair_cand_bytes(int64_t rows);
+cudaError_t launch_pair(const PairArgs& a, int BH, cudaStream_t st);
+
 struct AttnArgs {
   const int32_t* row_ptr;  // nullptr: dense (every key block)
   const int32_t* col_idx;
+  const uint32_t* pairs;   // tile list from launch_pair; nullptr: blocks (2p, 2p+1)
   uint16_t* o;             // bf16 bits
   float* lse;
   int32_t* dev_status;

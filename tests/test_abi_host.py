@@ -45,8 +45,11 @@ def test_sizes(sa):
     assert L.sa_num_blocks(ctypes.byref(p)) == 598
     assert L.sa_route_rows(ctypes.byref(p)) == 56 * 598
     assert L.sa_route_max_nnz(ctypes.byref(p)) == 56 * 598 * 598
-    vt = 56 * 128 * 38248 * 2
-    assert L.sa_attn_workspace_bytes(ctypes.byref(p)) == ((vt + 255) // 256) * 256 + 256
+    a256 = lambda x: (x + 255) // 256 * 256
+    vt = 56 * 128 * 38248 * 2                   # V repacked to fp16, key-contiguous
+    cand = 56 * 598 * 64 * 2                    # pairing: 64 candidates per block (int16)
+    tiles = 56 * 299 * 4                        # tile list
+    assert L.sa_attn_workspace_bytes(ctypes.byref(p)) == a256(vt) + 256 + a256(cand) + a256(tiles)
     assert L.sa_route_workspace_bytes(ctypes.byref(p)) > 56 * 598 * 598 * 4
     p1 = params(sa, S=1, H=1, D=64, P=0)
     assert L.sa_num_blocks(ctypes.byref(p1)) == 1

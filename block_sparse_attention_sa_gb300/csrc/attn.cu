@@ -618,6 +618,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           tmem_ld32(lane_base + s_col + half * 64, sr);
           tmem_ld32(lane_base + s_col + half * 64 + 32, sr + 32);
           tmem_wait_ld();
+          reg_fence64(sr);
           mask_tail(sr, e, Nb, last_valid);
           mx = max64(sr);
         }
@@ -661,6 +662,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
               uint32_t o[32];
               tmem_ld32(lane_base + o_col + 32 * cc, o);
               tmem_wait_ld();
+              reg_fence32(o);
 #pragma unroll
               for (int u = 0; u < 32; ++u) o[u] = __float_as_uint(__uint_as_float(o[u]) * alpha);
               tmem_st32(lane_base + o_col + 32 * cc, o);
@@ -692,6 +694,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         uint32_t ov[32];
         tmem_ld32(lane_base + o_col + 32 * cc, ov);
         tmem_wait_ld();
+        reg_fence32(ov);
         if (row_ok) {
 #pragma unroll
           for (int v = 0; v < 4; ++v) {

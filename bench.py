@@ -50,7 +50,7 @@ KERNELS_PER_STEP = 8  # pool, score, select, recheck, scan, emit, pack_v, attent
 # the ncu capture summarised under profiles/ (taken with 8 of the 56 heads and
 # scaled by 7: the traffic grows with the heads processed), valid only for the
 # attn.cu it was taken on (sha256 prefix); otherwise reported as null.
-ATTN_TRAFFIC = {"bytes": 2.200e9, "attn_cu_sha256": "6c11429ba1adcc79"}
+ATTN_TRAFFIC = {"bytes": 2.155e9, "attn_cu_sha256": "cbc7e39751b2e433"}
 
 
 def file_sha(path):

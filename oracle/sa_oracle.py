@@ -39,6 +39,20 @@ the docstrings below):
    log-sum-exp of the scaled logits. Non-causal. Padding tokens never enter.
 8. Dense attention = step 7 with every block kept.
 
+Two other readings of the router, selectable by ``mode`` (the pages leave the
+rule open; neither is the default):
+
+* "dense_prefix_queries": step 6 as above, and every query block that
+  intersects the prefix attends every key block (a reading of "compressed
+  prefix queries" in which the prefix rows are not routed at all).
+* "top_mass": step 6 keeps, besides the sink and the diagonal, the smallest
+  set of key blocks of largest p whose summed p reaches tau (tau a mass in
+  [0, 1]): blocks are ranked by p descending, equal p by index ascending, and
+  the block of rank r is kept iff the blocks ranked above it hold less than
+  tau (MiniAcc blog, "What is Sol attention?": Sol keeps the promising pairs
+  of each head). Cumulative sums within 1e-6 of tau, and p within 1e-6 of the
+  last kept block's across the cut, are ties.
+
 The parity of a Sol "correction term" for skipped pairs (MiniAcc blog, same
 section) is not pinned: the pages give no formula and it is not applied.
 """
@@ -120,6 +134,35 @@ def select_blocks(p: np.ndarray, tau: float, prefix_len: int,
     return kept | forced_mask(Nb, prefix_len, block)
 
 
+def select_top_mass(p: np.ndarray, tau: float) -> Tuple[np.ndarray, np.ndarray]:
+    """Top-mass reading of step 6, without the forced blocks.
+
+    For every row: rank the key blocks by p descending (equal p: lower index
+    first); the block of rank r is kept iff the blocks ranked above it sum to
+    less than tau. Returns (kept, ties), both [..., Nb] bool; ties marks the
+    decisions another correct implementation may take either way: a block
+    whose preceding mass is within 1e-6 of tau, and blocks whose p is within
+    1e-6 of the last kept block's p on the other side of the cut.
+    """
+    flat = p.reshape(-1, p.shape[-1])
+    kept = np.zeros(flat.shape, dtype=bool)
+    ties = np.zeros(flat.shape, dtype=bool)
+    idx = np.arange(flat.shape[1])
+    for r in range(flat.shape[0]):
+        row = flat[r]
+        order = np.lexsort((idx, -row))          # p descending, then index ascending
+        before = np.concatenate([[0.0], np.cumsum(row[order])[:-1]])
+        keep_rank = before < tau
+        kept[r, order[keep_rank]] = True
+        ties[r, order[np.abs(before - tau) <= TIE_WINDOW]] = True
+        n_keep = int(keep_rank.sum())
+        if 0 < n_keep < len(row):
+            p_last, p_next = row[order[n_keep - 1]], row[order[n_keep]]
+            if p_last - p_next <= TIE_WINDOW:     # the order across the cut is ambiguous
+                ties[r] |= (row >= p_next - TIE_WINDOW) & (row <= p_last + TIE_WINDOW)
+    return kept.reshape(p.shape), ties.reshape(p.shape)
+
+
 def threshold_ratio(p: np.ndarray, tau: float) -> np.ndarray:
     """p * Nb / tau: a block is kept by the router iff this is >= 1.
 
@@ -143,25 +186,43 @@ def to_csr(kept: np.ndarray) -> Tuple[np.ndarray, np.ndarray]:
     return row_ptr, col_idx
 
 
+ROUTE_MODES = ("threshold", "dense_prefix_queries", "top_mass")
+
+
 def route_ref(q, k, prefix_len: int, tau: float, scale: Optional[float] = None,
-              block: int = BLOCK) -> Dict[str, np.ndarray]:
+              block: int = BLOCK, mode: str = "threshold") -> Dict[str, np.ndarray]:
     """Steps 1-6: the block route of every (b, h, query block).
 
     Returns kept [B,H,Nb,Nb] bool, the CSR (row_ptr, col_idx), the pooled
-    softmax p, the threshold ratio and the forced mask.
+    softmax p, the forced mask (broadcast to kept's shape) and ties, the
+    decisions another correct router may take either way (never forced
+    ones). ``mode`` picks the reading of step 6 (module docstring).
     """
+    if mode not in ROUTE_MODES:
+        raise ValueError(f"unknown route mode {mode!r}")
     qf, kf = as_f64(q), as_f64(k)
     D = qf.shape[-1]
     scale = 1.0 / math.sqrt(D) if not scale else scale
     qbar, kbar = pool_blocks(qf, block), pool_blocks(kf, block)
     del qf, kf
     p = pooled_softmax(pooled_logits(qbar, kbar, scale))
-    kept = select_blocks(p, tau, prefix_len, block)
-    row_ptr, col_idx = to_csr(kept)
     Nb = p.shape[-1]
+    forced = np.broadcast_to(forced_mask(Nb, prefix_len, block), p.shape).copy()
+    if mode == "dense_prefix_queries":
+        n_sink = (prefix_len + block - 1) // block
+        forced[..., :n_sink, :] = True
+    if mode == "top_mass":
+        by_mass, ties = select_top_mass(p, tau)
+        kept = by_mass | forced
+        ratio = None
+    else:
+        kept = select_blocks(p, tau, prefix_len, block) | forced
+        ratio = threshold_ratio(p, tau)
+        ties = np.abs(ratio - 1.0) <= TIE_WINDOW
+    ties = ties & ~forced
+    row_ptr, col_idx = to_csr(kept)
     return {"kept": kept, "row_ptr": row_ptr, "col_idx": col_idx, "p": p,
-            "ratio": threshold_ratio(p, tau), "forced": forced_mask(Nb, prefix_len, block),
-            "qbar": qbar, "kbar": kbar}
+            "ratio": ratio, "forced": forced, "ties": ties, "qbar": qbar, "kbar": kbar}
 
 
 def block_density(kept: np.ndarray) -> float:

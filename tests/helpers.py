@@ -58,7 +58,7 @@ def compare_route(gpu_rp, gpu_ci, ref, B, H, Nb):
     """Returns (n_mismatch_outside_ties, n_ties)."""
     check_csr_wellformed(gpu_rp, gpu_ci, Nb)
     kept_gpu = kept_from_csr(gpu_rp, gpu_ci, B, H, Nb)
-    ties = oracle.tie_mask(ref["ratio"], np.broadcast_to(ref["forced"], ref["ratio"].shape))
+    ties = ref["ties"]
     diff = (kept_gpu != ref["kept"]) & ~ties
     return int(diff.sum()), int(ties.sum())
 

@@ -298,3 +298,77 @@ def test_generators_shapes_and_determinism():
     assert cfg.P + cfg.grid[0] * cfg.grid[1] * cfg.grid[2] == cfg.S
     cfg = sa_inputs.get_config("long")
     assert cfg.S - cfg.P == 110 * 24 * 42 + 809
+
+
+# ------------------------------------------------- router readings (modes) --
+
+def test_top_mass_hand_example():
+    # ranks: 0.5 (block 0), 0.2 (block 1), 0.2 (block 2: equal p, higher index), 0.1
+    p = np.array([[0.5, 0.2, 0.2, 0.1]])
+    kept, ties = oracle.select_top_mass(p, 0.6)          # 0 < .6, .5 < .6, .7 >= .6
+    assert kept[0].tolist() == [True, True, False, False]
+    assert ties[0].tolist() == [False, True, True, False]   # equal p across the cut
+    kept, ties = oracle.select_top_mass(p, 0.5)          # block 1 has 0.5 above it: not < 0.5
+    assert kept[0].tolist() == [True, False, False, False]
+    assert ties[0].tolist() == [False, True, False, False]  # its preceding mass equals tau
+    kept, _ = oracle.select_top_mass(p, 0.95)
+    assert kept[0].tolist() == [True, True, True, True]     # .9 above block 3 is < .95
+    kept, _ = oracle.select_top_mass(p, 0.0)
+    assert not kept.any()                                   # nothing holds less than 0
+    kept, ties = oracle.select_top_mass(np.array([[0.7, 0.3]]), 0.69)
+    assert kept[0].tolist() == [True, False] and not ties.any()
+
+
+def _brute_top_mass(row, tau):
+    order = sorted(range(len(row)), key=lambda j: (-row[j], j))
+    kept, acc = set(), 0.0
+    for j in order:
+        if acc < tau:
+            kept.add(j)
+        acc = math.fsum([acc, row[j]])
+    return kept
+
+
+def test_top_mass_against_brute_force_and_invariants():
+    rng = np.random.default_rng(5)
+    for trial in range(40):
+        n = int(rng.integers(2, 40))
+        s = rng.normal(size=n) * float(rng.uniform(0.1, 4.0))
+        p = np.exp(s - s.max())
+        p /= p.sum()
+        tau = float(rng.uniform(0.05, 0.99))
+        kept, ties = oracle.select_top_mass(p[None], tau)
+        kept, ties = kept[0], ties[0]
+        want = _brute_top_mass(p.tolist(), tau)
+        got = set(np.nonzero(kept)[0].tolist())
+        assert (got ^ want) <= set(np.nonzero(ties)[0].tolist())
+        if not ties.any():
+            assert got == want
+            assert p[kept].sum() >= tau - 1e-12                 # the kept blocks cover tau
+            assert p[kept].sum() - p[kept].min() < tau          # and none of them is spare
+        kept_hi, _ = oracle.select_top_mass(p[None], min(1.0, tau + 0.05))
+        assert not (kept & ~kept_hi[0]).any()                    # monotone in tau
+        perm = rng.permutation(n)                                # equivariant if no equal p
+        kp, _ = oracle.select_top_mass(p[perm][None], tau)
+        if not ties.any():
+            assert np.array_equal(kp[0], kept[perm])
+
+
+def test_route_modes_forced_blocks_and_prefix_rows():
+    q, k, _ = sa_inputs.random_small(700, 2, 64, seed=11)
+    P = 130                                     # 3 sink blocks
+    thr = oracle.route_ref(q, k, P, 1.0)
+    dpq = oracle.route_ref(q, k, P, 1.0, mode="dense_prefix_queries")
+    top = oracle.route_ref(q, k, P, 0.5, mode="top_mass")
+    n_sink, Nb = 3, oracle.num_blocks(700)
+    assert dpq["kept"][:, :, :n_sink, :].all()                 # prefix rows keep everything
+    assert np.array_equal(dpq["kept"][:, :, n_sink:], thr["kept"][:, :, n_sink:])
+    for r in (thr, dpq, top):
+        assert r["kept"][..., :n_sink].all()                    # sink columns
+        assert r["kept"][..., np.arange(Nb), np.arange(Nb)].all()   # diagonal
+        assert not (r["ties"] & r["forced"]).any()
+    # top-mass rows cover tau with their unforced-or-forced blocks
+    cover = (top["p"] * top["kept"]).sum(-1)
+    assert (cover >= 0.5 - 1e-12).all()
+    with pytest.raises(ValueError):
+        oracle.route_ref(q, k, P, 1.0, mode="z")

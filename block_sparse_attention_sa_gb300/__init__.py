@@ -28,6 +28,7 @@ __all__ = [
     "sa_attn_sparse", "sa_attn_dense", "sa_forward_host", "sa_route_workspace_bytes",
     "sa_attn_workspace_bytes", "sa_route_max_nnz", "check_dev_status", "EXPORTS",
     "SA_DEV_CAPACITY", "SA_DEV_TIMEOUT", "SA_DEV_BAD_ROUTE", "SA_DEV_RANGE",
+    "SA_ROUTE_THRESHOLD", "SA_ROUTE_DENSE_PREFIX_QUERIES", "SA_ROUTE_TOP_MASS", "ROUTE_MODES",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -35,6 +36,11 @@ _LIB = None
 
 SA_OK, SA_ERR_INVALID_ARG, SA_ERR_UNSUPPORTED, SA_ERR_CAPACITY, SA_ERR_CUDA, SA_ERR_TIMEOUT = range(6)
 SA_DEV_CAPACITY, SA_DEV_TIMEOUT, SA_DEV_BAD_ROUTE, SA_DEV_RANGE = 1, 2, 4, 8
+# readings of the router rule (sa_params.route_mode)
+SA_ROUTE_THRESHOLD, SA_ROUTE_DENSE_PREFIX_QUERIES, SA_ROUTE_TOP_MASS = 0, 1, 2
+ROUTE_MODES = {"threshold": SA_ROUTE_THRESHOLD,
+               "dense_prefix_queries": SA_ROUTE_DENSE_PREFIX_QUERIES,
+               "top_mass": SA_ROUTE_TOP_MASS}
 
 # Every function include/sa.h declares.
 EXPORTS = (
@@ -59,6 +65,7 @@ class sa_params(ctypes.Structure):
         ("tau", ctypes.c_float), ("softmax_scale", ctypes.c_float),
         ("q_stride", ctypes.c_int64 * 3), ("k_stride", ctypes.c_int64 * 3),
         ("v_stride", ctypes.c_int64 * 3), ("o_stride", ctypes.c_int64 * 3),
+        ("route_mode", ctypes.c_int32), ("reserved", ctypes.c_int32),
     ]
 
 
@@ -140,11 +147,12 @@ def _require_cuda(*ts):
 
 def make_params(q: torch.Tensor, k: Optional[torch.Tensor] = None, v: Optional[torch.Tensor] = None,
                 o: Optional[torch.Tensor] = None, prefix_len: int = 0, tau: float = 1.0,
-                scale: float = 0.0) -> sa_params:
+                scale: float = 0.0, mode="threshold") -> sa_params:
     B, S, H, D = q.shape
     p = sa_params()
     p.B, p.S, p.H, p.D, p.block = B, S, H, D, 64
     p.prefix_len, p.tau, p.softmax_scale = int(prefix_len), float(tau), float(scale)
+    p.route_mode = ROUTE_MODES[mode] if isinstance(mode, str) else int(mode)
     for field, t in (("q_stride", q), ("k_stride", k if k is not None else q),
                      ("v_stride", v if v is not None else q), ("o_stride", o if o is not None else q)):
         st = _bshd_strides(t, field[0])
@@ -175,15 +183,17 @@ def _workspace(nbytes: int, device, ws: Optional[torch.Tensor]) -> torch.Tensor:
 
 
 def sa_route(q: torch.Tensor, k: torch.Tensor, prefix_len: int, tau: float, scale: float = 0.0, *,
-             row_ptr: Optional[torch.Tensor] = None, col_idx: Optional[torch.Tensor] = None,
-             workspace: Optional[torch.Tensor] = None, dev_status: Optional[torch.Tensor] = None,
+             mode="threshold", row_ptr: Optional[torch.Tensor] = None,
+             col_idx: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+             dev_status: Optional[torch.Tensor] = None,
              stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
     """Block route of every (b, h, query block): int32 row_ptr [B*H*Nb+1] and
     col_idx (capacity B*H*Nb*Nb unless given; valid entries are
-    col_idx[:row_ptr[-1]])."""
+    col_idx[:row_ptr[-1]]). ``mode``: "threshold", "dense_prefix_queries" or
+    "top_mass" (the SA_ROUTE_* readings of sa.h)."""
     _require_cuda(q, k)
     lib = load_library()
-    p = make_params(q, k, prefix_len=prefix_len, tau=tau, scale=scale)
+    p = make_params(q, k, prefix_len=prefix_len, tau=tau, scale=scale, mode=mode)
     rows = int(lib.sa_route_rows(ctypes.byref(p)))
     if rows == 0:
         _check(SA_ERR_INVALID_ARG, "sa_route")

@@ -243,7 +243,10 @@ __global__ void __launch_bounds__(256) select_kernel(RouteArgs a) {
   int cnt = 0;
   bool flag = false;
 
-  if (a.keep_all) {
+  // rows that keep every key block: tau = 0 (outside top-mass), or a query
+  // block meeting the prefix when prefix query rows are dense
+  const bool row_all = a.keep_all || (a.mode == SA_ROUTE_DENSE_PREFIX_QUERIES && i < a.n_sink);
+  if (row_all) {
     for (int w = 0; w < a.words; ++w) {
       const int j = w * 32 + lane;
       const uint32_t m = __ballot_sync(full, j < a.Nb);
@@ -269,7 +272,70 @@ __global__ void __launch_bounds__(256) select_kernel(RouteArgs a) {
     // short shuffle-tree sums (relative 1e-6 of Z, so 1e-6 absolute in log Z),
     // logf (1 ulp of |log Z| <= 8) and three additions (ulps of |T|).
     const float err_row = gq * kmx + 2e-6f + 5e-7f * fabsf(T);
-    const float* srow = ws_ptr<float>(a.ws, a.L.scores) + row * a.Nb;
+    float* srow = ws_ptr<float>(a.ws, a.L.scores) + row * a.Nb;
+    if (a.mode == SA_ROUTE_TOP_MASS) {
+      // p_j in place of the logits (this kernel is their last reader), then
+      // a bisection on the cut: f(x) = sum of the p_j above x is decreasing;
+      // keep the p_j above lo, where f(lo) >= tau > f(hi) and hi - lo is
+      // below the spacing of distinct p. Rows whose fp32 masses at the cut,
+      // or whose p on either side of the cut, are within the error bound of
+      // tau or of each other go to the fp64 recheck.
+      const float lse = M + logf(Z);
+      for (int j = lane; j < a.Nb; j += 32) srow[j] = expf(srow[j] - lse);
+      __syncwarp();
+      auto mass_above = [&](float x) {
+        float f = 0.f;
+        for (int j = lane; j < a.Nb; j += 32) {
+          const float pj = srow[j];
+          f += pj > x ? pj : 0.f;
+        }
+        for (int off = 16; off >= 1; off >>= 1) f += __shfl_xor_sync(full, f, off);
+        return f;
+      };
+      // the logit error bound becomes a relative error of each p (twice:
+      // the logit and the log-sum-exp), plus the fp32 sums of up to Nb terms
+      const float bound = 4.f * (gq * kmx + err_row) + (a.Nb / 32 + 8) * 2.4e-7f;
+      float lo = 0.f, hi = 1.f, flo = 0.f, fhi = 0.f;
+      bool take_all = false, take_none = false;
+      if (a.tau <= 0.f) {
+        take_none = true;
+      } else {
+        flo = mass_above(0.f);
+        if (flo < a.tau) {
+          take_all = true;            // even every block falls short of tau
+          if (a.tau - flo <= bound) flag = true;
+        } else {
+          for (int itb = 0; itb < 40; ++itb) {
+            const float mid = 0.5f * (lo + hi);
+            const float fm = mass_above(mid);
+            if (fm >= a.tau) { lo = mid; flo = fm; }
+            else { hi = mid; fhi = fm; }
+          }
+          float p_last = INFINITY, p_next = 0.f;   // smallest kept, largest dropped
+          for (int j = lane; j < a.Nb; j += 32) {
+            const float pj = srow[j];
+            if (pj > lo) p_last = fminf(p_last, pj);
+            else p_next = fmaxf(p_next, pj);
+          }
+          for (int off = 16; off >= 1; off >>= 1) {
+            p_last = fminf(p_last, __shfl_xor_sync(full, p_last, off));
+            p_next = fmaxf(p_next, __shfl_xor_sync(full, p_next, off));
+          }
+          if (flo - a.tau <= bound || a.tau - fhi <= bound || p_last - p_next <= bound) flag = true;
+        }
+      }
+      for (int w = 0; w < a.words; ++w) {
+        const int j = w * 32 + lane;
+        bool keep = false;
+        if (j < a.Nb) {
+          const bool forced = (j < a.n_sink) || (j == i);
+          keep = forced || take_all || (!take_none && srow[j] > lo);
+        }
+        const uint32_t m = __ballot_sync(full, keep);
+        if (lane == 0) bits[w] = m;
+        cnt += __popc(m);
+      }
+    } else {
     for (int w = 0; w < a.words; ++w) {
       const int j = w * 32 + lane;
       bool keep = false;
@@ -282,6 +348,7 @@ __global__ void __launch_bounds__(256) select_kernel(RouteArgs a) {
       const uint32_t m = __ballot_sync(full, keep);
       if (lane == 0) bits[w] = m;
       cnt += __popc(m);
+    }
     }
   }
   flag = __any_sync(full, flag);
@@ -337,6 +404,37 @@ __global__ void __launch_bounds__(128) recheck_kernel(RouteArgs a) {
     if (lane == 0) red[warp] = z;
     __syncthreads();
     z = (red[0] + red[1]) + (red[2] + red[3]);
+    __syncthreads();
+    // top-mass: the same bisection as the select kernel, in fp64 on the fp64
+    // softmax (blocks above lo are kept, f(lo) >= tau > f(hi))
+    double lo = 0.0;
+    bool take_all = false, take_none = false;
+    if (a.mode == SA_ROUTE_TOP_MASS) {
+      for (int k = threadIdx.x; k < a.Nb; k += 128) s64[k] = exp(s64[k] - m) / z;
+      __syncthreads();
+      auto mass_above = [&](double x) {
+        double f = 0.0;
+        for (int k = threadIdx.x; k < a.Nb; k += 128) f += s64[k] > x ? s64[k] : 0.0;
+        for (int off = 16; off >= 1; off >>= 1) f += __shfl_xor_sync(full, f, off);
+        if (lane == 0) red[warp] = f;
+        __syncthreads();
+        f = (red[0] + red[1]) + (red[2] + red[3]);
+        __syncthreads();
+        return f;
+      };
+      if (a.tau64 <= 0.0) {
+        take_none = true;
+      } else if (mass_above(0.0) < a.tau64) {
+        take_all = true;
+      } else {
+        double hi = 1.0;
+        for (int itb = 0; itb < 64; ++itb) {
+          const double mid = 0.5 * (lo + hi);
+          if (mass_above(mid) >= a.tau64) lo = mid;
+          else hi = mid;
+        }
+      }
+    }
     uint32_t* bits = ws_ptr<uint32_t>(a.ws, a.L.bits) + row * a.words;
     int cnt = 0;
     for (int w = warp; w < a.words; w += 4) {
@@ -344,7 +442,10 @@ __global__ void __launch_bounds__(128) recheck_kernel(RouteArgs a) {
       bool keep = false;
       if (j < a.Nb) {
         const bool forced = (j < a.n_sink) || (j == i);
-        keep = forced || (exp(s64[j] - m) / z >= a.tau_over_nb);
+        if (a.mode == SA_ROUTE_TOP_MASS)
+          keep = forced || take_all || (!take_none && s64[j] > lo);
+        else
+          keep = forced || (exp(s64[j] - m) / z >= a.tau_over_nb);
       }
       const uint32_t bm = __ballot_sync(full, keep);
       if (lane == 0) bits[w] = bm;

@@ -42,6 +42,9 @@ sa_status check_params(const sa_params* p) {
   if (p->prefix_len < 0 || p->prefix_len > p->S) return SA_ERR_INVALID_ARG;
   if (!(p->tau >= 0.f) || !std::isfinite(p->tau)) return SA_ERR_INVALID_ARG;
   if (!(p->softmax_scale >= 0.f) || !std::isfinite(p->softmax_scale)) return SA_ERR_INVALID_ARG;
+  if (p->route_mode < SA_ROUTE_THRESHOLD || p->route_mode > SA_ROUTE_TOP_MASS || p->reserved != 0)
+    return SA_ERR_INVALID_ARG;
+  if (p->route_mode == SA_ROUTE_TOP_MASS && p->tau > 1.f) return SA_ERR_INVALID_ARG;
   if (p->D != 64 && p->D != 128) return p->D > 0 ? SA_ERR_UNSUPPORTED : SA_ERR_INVALID_ARG;
   if (p->H > 65535 || p->B > 65535) return SA_ERR_UNSUPPORTED;
   const int64_t nb = num_blocks(p->S);
@@ -264,9 +267,12 @@ sa_status sa_route(const sa_params* p, const void* q, const void* k, int32_t* ro
   a.n_sink = (p->prefix_len + kBlock - 1) / kBlock;
   a.scale64 = scale64_of(p);
   a.scale = static_cast<float>(a.scale64);
-  a.keep_all = p->tau == 0.f;
+  a.mode = p->route_mode;
+  a.tau = p->tau;
+  a.tau64 = static_cast<double>(p->tau);
+  a.keep_all = p->route_mode != SA_ROUTE_TOP_MASS && p->tau == 0.f;
   a.tau_over_nb = static_cast<double>(p->tau) / L.Nb;
-  a.log_tau_over_nb = a.keep_all ? 0.f
+  a.log_tau_over_nb = (a.keep_all || p->tau == 0.f) ? 0.f
                                  : static_cast<float>(std::log(static_cast<double>(p->tau)) -
                                                       std::log(static_cast<double>(L.Nb)));
   // gamma_n (1 + 1%) with u = 2^-24 and n = 16 + D/16 + 3: the score kernel

@@ -36,7 +36,10 @@ struct RouteArgs {
   double scale64;         // fp64 softmax scale
   float log_tau_over_nb;  // logf(tau) - logf(Nb)  (tau > 0)
   double tau_over_nb;     // tau / Nb in fp64
-  int keep_all;           // tau == 0
+  int keep_all;           // tau == 0 outside SA_ROUTE_TOP_MASS
+  int mode;               // SA_ROUTE_*
+  float tau;              // top-mass: the mass to reach
+  double tau64;
   float gamma;            // fp32 dot-product error constant
   char* ws;
   RouteLayout L;

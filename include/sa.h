@@ -61,20 +61,35 @@ enum {
                                P.V product runs in fp16, see sa_attn_sparse    */
 };
 
+/* Readings of the router rule (sa_route; the pages leave the rule open). */
+enum {
+  SA_ROUTE_THRESHOLD = 0,           /* keep p_ij >= tau / Nb (the default)     */
+  SA_ROUTE_DENSE_PREFIX_QUERIES = 1,/* as THRESHOLD, and every query block that
+                                       meets the prefix keeps every key block */
+  SA_ROUTE_TOP_MASS = 2             /* keep the fewest key blocks of largest
+                                       p_ij whose summed p_ij reaches tau     */
+};
+
 typedef struct sa_params {
   int32_t B, S, H, D;     /* D must be 64 or 128; B, S, H >= 1               */
   int32_t block;          /* must be 64                                       */
   int32_t prefix_len;     /* P, 0 <= P <= S: key tokens [0, P) are always
                              attended, via every key block j < ceil(P/64)    */
-  float tau;              /* router threshold, >= 0; 0 keeps every block     */
+  float tau;              /* router parameter, >= 0: for THRESHOLD and
+                             DENSE_PREFIX_QUERIES a multiple of the uniform
+                             share (0 keeps every block); for TOP_MASS a mass
+                             in [0, 1] (0 keeps only the forced blocks)      */
   float softmax_scale;    /* 0 => 1/sqrt(D); used for routing and attention  */
   int64_t q_stride[3];    /* element strides of b, s, h (d is contiguous)    */
   int64_t k_stride[3];
   int64_t v_stride[3];
   int64_t o_stride[3];
+  int32_t route_mode;     /* SA_ROUTE_*; sa_params_init sets THRESHOLD       */
+  int32_t reserved;       /* must be 0                                        */
 } sa_params;
 
-/* Fills p for a contiguous [B, S, H, D] layout of all four tensors. */
+/* Fills p for a contiguous [B, S, H, D] layout of all four tensors, with
+ * route_mode = SA_ROUTE_THRESHOLD and softmax_scale = 0. */
 void sa_params_init(sa_params* p, int32_t B, int32_t S, int32_t H, int32_t D,
                     int32_t prefix_len, float tau);
 
@@ -101,10 +116,17 @@ size_t sa_route_workspace_bytes(const sa_params* p);
  *   s_ij = softmax_scale * qbar_i . kbar_j for every key block j;
  *   p_ij = softmax over j of s_ij;
  *   keep j  iff  p_ij >= tau / Nb,  or j < ceil(P/64) (sink),  or j == i.
- * Decisions match an fp64 evaluation of the rule except where
- * |p_ij * Nb / tau - 1| <= 1e-6 (ties). Pooling is exact to fp64 rounding;
- * the scores are computed in fp32 and every row holding a decision whose
- * fp32 margin is inside a rigorous error bound is recomputed in fp64.
+ * p->route_mode selects another reading: DENSE_PREFIX_QUERIES also keeps
+ * every key block of query blocks i < ceil(P/64); TOP_MASS replaces the
+ * first test by: rank the key blocks by p_ij descending (equal p_ij: lower j
+ * first) and keep block j iff the blocks ranked above it sum to less than
+ * tau.
+ * Decisions match an fp64 evaluation of the rule except on ties: for
+ * THRESHOLD, |p_ij * Nb / tau - 1| <= 1e-6; for TOP_MASS, a preceding mass
+ * within 1e-6 of tau, or p_ij within 1e-6 of the last kept block's across the
+ * cut. Pooling is exact to fp64 rounding; the scores are computed in fp32
+ * and every row holding a decision inside a rigorous fp32 error bound is
+ * recomputed in fp64.
  *
  * q, k       device, bf16 [B, S, H, D] with the strides in p; not modified.
  * row_ptr    device int32 [B*H*Nb + 1]; row r = (b*H + h)*Nb + i.

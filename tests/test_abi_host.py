@@ -58,7 +58,8 @@ def test_sizes(sa):
 @pytest.mark.parametrize("field,value,code", [
     ("D", 96, 2), ("D", 0, 1), ("block", 32, 1), ("S", 0, 1), ("prefix_len", -1, 1),
     ("prefix_len", 40000, 1), ("tau", -1.0, 1), ("tau", float("inf"), 1), ("H", 0, 1),
-    ("softmax_scale", float("nan"), 1),
+    ("softmax_scale", float("nan"), 1), ("route_mode", 3, 1), ("route_mode", -1, 1),
+    ("reserved", 1, 1),
 ])
 def test_bad_params_rejected_before_launch(sa, field, value, code):
     L = sa.load_library()
@@ -70,6 +71,23 @@ def test_bad_params_rejected_before_launch(sa, field, value, code):
     assert L.sa_attn_dense(ctypes.byref(p), dummy, dummy, dummy, dummy, None, dummy, 1 << 40,
                            None, None) == code
     assert L.sa_route_workspace_bytes(ctypes.byref(p)) == 0
+
+
+def test_route_modes_and_their_tau_ranges(sa):
+    L = sa.load_library()
+    p = params(sa)
+    assert p.route_mode == sa.SA_ROUTE_THRESHOLD           # what sa_params_init sets
+    assert L.sa_route_workspace_bytes(ctypes.byref(p)) > 0
+    p.route_mode = sa.SA_ROUTE_TOP_MASS
+    p.tau = 1.0                                            # a mass: at most 1
+    assert L.sa_route_workspace_bytes(ctypes.byref(p)) > 0
+    p.tau = 1.5
+    assert L.sa_route_workspace_bytes(ctypes.byref(p)) == 0
+    dummy = ctypes.c_void_p(256)
+    assert L.sa_route(ctypes.byref(p), dummy, dummy, dummy, dummy, 10, dummy, 1 << 40,
+                      None, None) == 1
+    p.route_mode = sa.SA_ROUTE_DENSE_PREFIX_QUERIES         # a multiple of 1/Nb: any tau >= 0
+    assert L.sa_route_workspace_bytes(ctypes.byref(p)) > 0
 
 
 def test_null_and_misaligned_pointers_rejected(sa):

@@ -44,7 +44,11 @@ import sa_inputs  # noqa: E402
 
 METRIC = "ms/layer and effective TFLOP/s (% of GB300 bf16 peak) at S=38,247, ~18% density"
 UNIT = "TFLOP/s"
-KERNELS_PER_STEP = 8  # pool, score, select, recheck, scan, emit, pack_v, attention
+# our kernels per step: the router (pool, score, select, recheck, scan, emit),
+# then the tile pairing (pair_rank, pair_match; only when there are more than
+# two query blocks), the V repack and the attention kernel; dense mode runs
+# just the last two
+ROUTE_KERNELS, PAIR_KERNELS, ATTN_KERNELS = 6, 2, 2
 
 # DRAM traffic of one attention-kernel launch at the release workload, from
 # the ncu capture summarised under profiles/ (taken with 8 of the 56 heads and
@@ -190,6 +194,8 @@ def run_ours(args):
     sa.load_library()
 
     cfg = sa_inputs.get_config(args.workload, **({"H": args.heads} if args.heads else {}))
+    tau = cfg.tau if args.tau is None else args.tau
+    mode = args.route_mode
     q, k, v = sa_inputs.make_qkv(cfg)
     B, S, H, D = q.shape
     qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
@@ -203,8 +209,8 @@ def run_ours(args):
         if ev is not None:
             ev[0].record(stream)
         if not dense:
-            sa.sa_route(qd, kd, cfg.P, cfg.tau, row_ptr=rp_buf, col_idx=ci_buf, workspace=ws,
-                        dev_status=status)
+            sa.sa_route(qd, kd, cfg.P, tau, mode=mode, row_ptr=rp_buf, col_idx=ci_buf,
+                        workspace=ws, dev_status=status)
         if ev is not None:
             ev[1].record(stream)
         if dense:
@@ -256,7 +262,9 @@ def run_ours(args):
                if ATTN_TRAFFIC["attn_cu_sha256"] and sha.startswith(ATTN_TRAFFIC["attn_cu_sha256"])
                else None)
 
-    e2e = None if args.no_e2e else run_e2e(sa, cfg, q, k, v, bufs, flops, args, world, dev, stream)
+    e2e = None if args.no_e2e else run_e2e(sa, cfg, q, k, v, bufs, flops, args, world, dev,
+                                           stream, tau, mode)
+    per_step = ATTN_KERNELS + (0 if dense else ROUTE_KERNELS + (PAIR_KERNELS if Nb > 2 else 0))
 
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
@@ -264,7 +272,8 @@ def run_ours(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded; stands in for the model's activations)",
         "config": {"workload": cfg.name, "B": B, "S": S, "H": H, "D": D, "prefix": cfg.P,
-                   "tau": cfg.tau, "block": 64, "density": round(density, 5),
+                   "tau": tau, "route_mode": "dense" if dense else mode, "block": 64,
+                   "density": round(density, 5),
                    "routed_tflop_per_layer": round(flops / 1e12, 4),
                    "ms_route": round(statistics.mean(route_ms), 4),
                    "ms_attn": round(attn_avg, 4),
@@ -275,12 +284,13 @@ def run_ours(args):
                      "frac": round(achieved / peak, 4),
                      "peak_kind": f"{'sustained' if long_region else 'burst'} bf16, {peak_src}",
                      "traffic": traffic},
-        "gpu_launches": KERNELS_PER_STEP * args.steps,
+        "gpu_launches": per_step * args.steps,
         "e2e": e2e,
         "clocks": clk.summary(),
     }
     if world == 1 and not args.no_cpu and rank == 0:
-        result["cpu_baseline"] = cpu_baseline(cfg, q, k, v, flops, budget_s=15.0)
+        result["cpu_baseline"] = cpu_baseline(cfg, q, k, v, flops, budget_s=15.0, tau=tau,
+                                              mode=mode)
     if rank == 0:
         print(json.dumps(result), flush=True)
     if world > 1:
@@ -288,21 +298,21 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def run_e2e(sa, cfg, q, k, v, bufs, flops, args, world, dev, stream):
+def run_e2e(sa, cfg, q, k, v, bufs, flops, args, world, dev, stream, tau, mode):
     """The same layer through sa_forward_host: pinned host Q/K/V in, host O out,
     copies inside the timed region."""
     qh, kh, vh = (t.contiguous().pin_memory() for t in (q, k, v))
     oh = torch.empty_like(qh, pin_memory=True)
     steps = max(3, min(args.steps, 10))
     for _ in range(2):
-        sa.sa_forward_host(qh, kh, vh, cfg.P, cfg.tau, bufs=bufs, o_host=oh)
+        sa.sa_forward_host(qh, kh, vh, cfg.P, tau, bufs=bufs, mode=mode, o_host=oh)
     torch.cuda.synchronize()
     s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize()
     s.record(stream)
     for _ in range(steps):
-        sa.sa_forward_host(qh, kh, vh, cfg.P, cfg.tau, bufs=bufs, o_host=oh)
+        sa.sa_forward_host(qh, kh, vh, cfg.P, tau, bufs=bufs, mode=mode, o_host=oh)
     e.record(stream)
     torch.cuda.synchronize()
     ms = timed_max_ms(s.elapsed_time(e), steps, world, dev)
@@ -314,7 +324,7 @@ def run_e2e(sa, cfg, q, k, v, bufs, flops, args, world, dev, stream):
 
 # ------------------------------------------------------- the CPU oracle ----
 
-def cpu_baseline(cfg, q, k, v, flops, budget_s=15.0, seed=0):
+def cpu_baseline(cfg, q, k, v, flops, budget_s=15.0, seed=0, tau=None, mode="threshold"):
     """Time the oracle on a bounded sample of the layer and scale to a whole
     layer: the route of one head in full, plus as many query blocks of that
     head as fit in ``budget_s`` (at least 4), extrapolated linearly to all
@@ -327,7 +337,8 @@ def cpu_baseline(cfg, q, k, v, flops, budget_s=15.0, seed=0):
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
     qs, ks, vs = (t[:, :, h:h + 1].contiguous() for t in (q, k, v))
     t0 = time.perf_counter()
-    r = oracle.route_ref(qs, ks, cfg.P, float(np.float32(cfg.tau)))
+    tau = cfg.tau if tau is None else tau
+    r = oracle.route_ref(qs, ks, cfg.P, float(np.float32(tau)), mode=mode)
     t_route = time.perf_counter() - t0
     order = np.random.default_rng(seed).permutation(Nb)
     t_attn, n_done = 0.0, 0
@@ -350,16 +361,18 @@ def run_reference(args):
     if rank != 0:
         return
     cfg = sa_inputs.get_config(args.workload)
+    tau = cfg.tau if args.tau is None else args.tau
+    mode = args.route_mode
     q, k, v = sa_inputs.make_qkv(cfg)
     B, S, H, D = q.shape
     import oracle
     # the layer's routed FLOPs from the oracle's own route
-    ref = oracle.route_ref(q, k, cfg.P, float(np.float32(cfg.tau)))
+    ref = oracle.route_ref(q, k, cfg.P, float(np.float32(tau)), mode=mode)
     flops = routed_flops(ref["row_ptr"], ref["col_idx"], B, H, S, D)
     del ref
     for w in range(args.warmup):
-        cpu_baseline(cfg, q, k, v, flops, budget_s=1.0, seed=w)
-    vals = [cpu_baseline(cfg, q, k, v, flops, budget_s=5.0, seed=100 + s)
+        cpu_baseline(cfg, q, k, v, flops, budget_s=1.0, seed=w, tau=tau, mode=mode)
+    vals = [cpu_baseline(cfg, q, k, v, flops, budget_s=5.0, seed=100 + s, tau=tau, mode=mode)
             for s in range(args.steps)]
     value = statistics.mean(c["value"] for c in vals)
     ms = flops / (value * 1e12) * 1e3
@@ -369,7 +382,7 @@ def run_reference(args):
         "ms_per_step": round(ms, 1), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
         "config": {"workload": cfg.name, "B": B, "S": S, "H": H, "D": D, "prefix": cfg.P,
-                   "tau": cfg.tau},
+                   "tau": tau, "route_mode": mode},
         "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": vals[0]["cores"],
                          "kind": "oracle", "sample": vals[-1]["sample"]},
         "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -386,6 +399,10 @@ def main():
     ap.add_argument("--workload", default="release", choices=sorted(sa_inputs.CONFIGS))
     ap.add_argument("--heads", type=int, default=0,
                     help="override H (smaller captures for profiling)")
+    ap.add_argument("--route-mode", default="threshold",
+                    choices=["threshold", "dense_prefix_queries", "top_mass"],
+                    help="reading of the router rule (sa.h SA_ROUTE_*)")
+    ap.add_argument("--tau", type=float, default=None, help="override the workload's tau")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     args = ap.parse_args()

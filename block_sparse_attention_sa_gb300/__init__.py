@@ -255,15 +255,15 @@ def sa_attn_dense(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: floa
 
 def sa_forward_host(q_host: torch.Tensor, k_host: torch.Tensor, v_host: torch.Tensor,
                     prefix_len: int, tau: float, scale: float = 0.0, *, bufs: dict,
-                    o_host: Optional[torch.Tensor] = None, lse_host: Optional[torch.Tensor] = None,
-                    stream=None) -> torch.Tensor:
+                    mode="threshold", o_host: Optional[torch.Tensor] = None,
+                    lse_host: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
     """One layer from (pinned) host tensors through the device buffers in
     ``bufs`` (q, k, v, o, lse, row_ptr, col_idx, ws, status); returns o_host.
     Enqueues only; synchronise the stream before reading o_host."""
     lib = load_library()
     if o_host is None:
         o_host = torch.empty_like(q_host, pin_memory=True)
-    p = make_params(bufs["q"], prefix_len=prefix_len, tau=tau, scale=scale)
+    p = make_params(bufs["q"], prefix_len=prefix_len, tau=tau, scale=scale, mode=mode)
     ws = bufs["ws"]
     code = lib.sa_forward_host(
         ctypes.byref(p), _ptr(q_host), _ptr(k_host), _ptr(v_host), _ptr(o_host), _ptr(lse_host),

@@ -321,7 +321,12 @@ __global__ void __launch_bounds__(256) select_kernel(RouteArgs a) {
             p_last = fminf(p_last, __shfl_xor_sync(full, p_last, off));
             p_next = fmaxf(p_next, __shfl_xor_sync(full, p_next, off));
           }
-          if (flo - a.tau <= bound || a.tau - fhi <= bound || p_last - p_next <= bound) flag = true;
+          // masses: absolute error <= bound; order across the cut: each p carries a
+          // relative error of about twice the logit bound, so a relative gap
+          // below twice that may be an inversion
+          const float rel = 4.f * (gq * kmx + err_row) + 4e-7f;
+          if (flo - a.tau <= bound || a.tau - fhi <= bound || p_last - p_next <= rel * p_last)
+            flag = true;
         }
       }
       for (int w = 0; w < a.words; ++w) {
@@ -412,28 +417,37 @@ __global__ void __launch_bounds__(128) recheck_kernel(RouteArgs a) {
     if (a.mode == SA_ROUTE_TOP_MASS) {
       for (int k = threadIdx.x; k < a.Nb; k += 128) s64[k] = exp(s64[k] - m) / z;
       __syncthreads();
-      auto mass_above = [&](double x) {
-        double f = 0.0;
-        for (int k = threadIdx.x; k < a.Nb; k += 128) f += s64[k] > x ? s64[k] : 0.0;
-        for (int off = 16; off >= 1; off >>= 1) f += __shfl_xor_sync(full, f, off);
-        if (lane == 0) red[warp] = f;
-        __syncthreads();
-        f = (red[0] + red[1]) + (red[2] + red[3]);
-        __syncthreads();
-        return f;
-      };
-      if (a.tau64 <= 0.0) {
-        take_none = true;
-      } else if (mass_above(0.0) < a.tau64) {
-        take_all = true;
-      } else {
-        double hi = 1.0;
-        for (int itb = 0; itb < 64; ++itb) {
-          const double mid = 0.5 * (lo + hi);
-          if (mass_above(mid) >= a.tau64) lo = mid;
-          else hi = mid;
+      // one warp bisects (shuffle sums only); the others wait at the barrier
+      if (warp == 0) {
+        auto mass_above = [&](double x) {
+          double f = 0.0;
+          for (int k = lane; k < a.Nb; k += 32) f += s64[k] > x ? s64[k] : 0.0;
+          for (int off = 16; off >= 1; off >>= 1) f += __shfl_xor_sync(full, f, off);
+          return f;
+        };
+        int state = 0;                          // 0: cut at lo, 1: keep all, 2: keep none
+        if (a.tau64 <= 0.0) {
+          state = 2;
+        } else if (mass_above(0.0) < a.tau64) {
+          state = 1;
+        } else {
+          double hi = 1.0;
+          for (int itb = 0; itb < 64; ++itb) {
+            const double mid = 0.5 * (lo + hi);
+            if (mass_above(mid) >= a.tau64) lo = mid;
+            else hi = mid;
+          }
+        }
+        if (lane == 0) {
+          red[0] = lo;
+          redc[0] = state;
         }
       }
+      __syncthreads();
+      lo = red[0];
+      take_all = redc[0] == 1;
+      take_none = redc[0] == 2;
+      __syncthreads();
     }
     uint32_t* bits = ws_ptr<uint32_t>(a.ws, a.L.bits) + row * a.words;
     int cnt = 0;

@@ -123,8 +123,8 @@ size_t sa_route_workspace_bytes(const sa_params* p);
  * tau.
  * Decisions match an fp64 evaluation of the rule except on ties: for
  * THRESHOLD, |p_ij * Nb / tau - 1| <= 1e-6; for TOP_MASS, a preceding mass
- * within 1e-6 of tau, or p_ij within 1e-6 of the last kept block's across the
- * cut. Pooling is exact to fp64 rounding; the scores are computed in fp32
+ * within 1e-6 of tau, or p_ij within a relative 1e-6 of the last kept
+ * block's across the cut. Pooling is exact to fp64 rounding; the scores are computed in fp32
  * and every row holding a decision inside a rigorous fp32 error bound is
  * recomputed in fp64.
  *

@@ -50,8 +50,8 @@ rule open; neither is the default):
   [0, 1]): blocks are ranked by p descending, equal p by index ascending, and
   the block of rank r is kept iff the blocks ranked above it hold less than
   tau (MiniAcc blog, "What is Sol attention?": Sol keeps the promising pairs
-  of each head). Cumulative sums within 1e-6 of tau, and p within 1e-6 of the
-  last kept block's across the cut, are ties.
+  of each head). Cumulative sums within 1e-6 of tau, and p within a relative
+  1e-6 of the last kept block's across the cut, are ties.
 
 The parity of a Sol "correction term" for skipped pairs (MiniAcc blog, same
 section) is not pinned: the pages give no formula and it is not applied.
@@ -141,8 +141,9 @@ def select_top_mass(p: np.ndarray, tau: float) -> Tuple[np.ndarray, np.ndarray]:
     first); the block of rank r is kept iff the blocks ranked above it sum to
     less than tau. Returns (kept, ties), both [..., Nb] bool; ties marks the
     decisions another correct implementation may take either way: a block
-    whose preceding mass is within 1e-6 of tau, and blocks whose p is within
-    1e-6 of the last kept block's p on the other side of the cut.
+    whose preceding mass is within 1e-6 of tau, and, when the p on either
+    side of the cut differ by at most 1e-6 of the last kept block's p, the
+    blocks whose p lies that close to the cut.
     """
     flat = p.reshape(-1, p.shape[-1])
     kept = np.zeros(flat.shape, dtype=bool)
@@ -158,8 +159,9 @@ def select_top_mass(p: np.ndarray, tau: float) -> Tuple[np.ndarray, np.ndarray]:
         n_keep = int(keep_rank.sum())
         if 0 < n_keep < len(row):
             p_last, p_next = row[order[n_keep - 1]], row[order[n_keep]]
-            if p_last - p_next <= TIE_WINDOW:     # the order across the cut is ambiguous
-                ties[r] |= (row >= p_next - TIE_WINDOW) & (row <= p_last + TIE_WINDOW)
+            w = TIE_WINDOW * p_last
+            if p_last - p_next <= w:              # the order across the cut is ambiguous
+                ties[r] |= (row >= p_next - w) & (row <= p_last + w)
     return kept.reshape(p.shape), ties.reshape(p.shape)
 
 

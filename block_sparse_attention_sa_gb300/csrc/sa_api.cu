@@ -1,6 +1,7 @@
 // sa_api.cu -- the extern "C" boundary: argument checks, workspace layout,
 // TMA descriptor encoding and the launch sequence of each entry point.
 #include <cmath>
+#include <algorithm>
 #include <cstring>
 #include <mutex>
 
@@ -185,6 +186,35 @@ sa_status attn_common(const sa_params* p, const void* q, const void* k, const vo
   return from_cuda(launch_attn(p->D, maps, a, st));
 }
 
+// sa_forward_host's copy streams and events, created on first use on each
+// device and kept until the process exits.
+constexpr int kHostGroups = 8;
+struct HostPipe {
+  std::mutex mu;
+  cudaStream_t h2d = nullptr, d2h = nullptr;
+  cudaEvent_t start = nullptr, end = nullptr, in[kHostGroups] = {}, done[kHostGroups] = {};
+  bool ok = false;
+};
+
+HostPipe* host_pipe(int dev) {
+  constexpr int kMaxDevices = 64;
+  static HostPipe pipes[kMaxDevices];
+  static std::once_flag once[kMaxDevices];
+  if (dev < 0 || dev >= kMaxDevices) return nullptr;
+  HostPipe& hp = pipes[dev];
+  std::call_once(once[dev], [&hp] {
+    bool ok = cudaStreamCreateWithFlags(&hp.h2d, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaStreamCreateWithFlags(&hp.d2h, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaEventCreateWithFlags(&hp.start, cudaEventDisableTiming) == cudaSuccess &&
+              cudaEventCreateWithFlags(&hp.end, cudaEventDisableTiming) == cudaSuccess;
+    for (int g = 0; ok && g < kHostGroups; ++g)
+      ok = cudaEventCreateWithFlags(&hp.in[g], cudaEventDisableTiming) == cudaSuccess &&
+           cudaEventCreateWithFlags(&hp.done[g], cudaEventDisableTiming) == cudaSuccess;
+    hp.ok = ok;
+  });
+  return hp.ok ? &hp : nullptr;
+}
+
 }  // namespace
 }  // namespace sa
 
@@ -319,24 +349,73 @@ sa_status sa_forward_host(const sa_params* p, const void* q_host, const void* k_
     if (p->q_stride[i] != cont[i] || p->k_stride[i] != cont[i] || p->v_stride[i] != cont[i] ||
         p->o_stride[i] != cont[i])
       return SA_ERR_INVALID_ARG;
-  const size_t bytes = static_cast<size_t>(p->B) * cont[0] * 2;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (cudaMemcpyAsync(q_dev, q_host, bytes, cudaMemcpyHostToDevice, st) != cudaSuccess ||
-      cudaMemcpyAsync(k_dev, k_host, bytes, cudaMemcpyHostToDevice, st) != cudaSuccess ||
-      cudaMemcpyAsync(v_dev, v_host, bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SA_ERR_CUDA;
+  HostPipe* hp = host_pipe(dev);
+  if (!hp) return SA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(hp->mu);
+
+  // Head groups: group g's route and attention start as soon as its Q, K, V
+  // slices are on the device and its O slice leaves as soon as it is done,
+  // so the copies of one group overlap the compute of the others (H2D and
+  // D2H on their own streams, compute on `stream`).
+  // (lse is [B, H, S]: a head group's rows are one contiguous slice only for
+  // B = 1, so a batched call that wants lse runs as a single group)
+  const int G = (p->B > 1 && lse_dev) ? 1 : std::max(1, std::min(kHostGroups, p->H / 8));
+  const size_t row_bytes = static_cast<size_t>(p->H) * p->D * 2;   // one token, all heads
+  const size_t rows = static_cast<size_t>(p->B) * p->S;
+  auto head0 = [&](int g) { return static_cast<int>(static_cast<int64_t>(p->H) * g / G); };
+  if (cudaEventRecord(hp->start, st) != cudaSuccess ||
+      cudaStreamWaitEvent(hp->h2d, hp->start, 0) != cudaSuccess ||
+      cudaStreamWaitEvent(hp->d2h, hp->start, 0) != cudaSuccess)
     return SA_ERR_CUDA;
-  s = sa_route(p, q_dev, k_dev, row_ptr, col_idx, col_cap, workspace, ws_bytes, dev_status, stream);
-  if (s != SA_OK) return s;
-  s = sa_attn_sparse(p, q_dev, k_dev, v_dev, row_ptr, col_idx, o_dev, lse_dev, workspace, ws_bytes,
-                     dev_status, stream);
-  if (s != SA_OK) return s;
-  if (cudaMemcpyAsync(o_host, o_dev, bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
-    return SA_ERR_CUDA;
-  if (lse_host && lse_dev) {
-    const size_t lb = static_cast<size_t>(p->B) * p->H * p->S * sizeof(float);
-    if (cudaMemcpyAsync(lse_host, lse_dev, lb, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+  for (int g = 0; g < G; ++g) {
+    const size_t off = static_cast<size_t>(head0(g)) * p->D * 2;
+    const size_t width = static_cast<size_t>(head0(g + 1) - head0(g)) * p->D * 2;
+    const void* src[3] = {q_host, k_host, v_host};
+    void* dst[3] = {q_dev, k_dev, v_dev};
+    for (int t = 0; t < 3; ++t)
+      if (cudaMemcpy2DAsync(static_cast<char*>(dst[t]) + off, row_bytes,
+                            static_cast<const char*>(src[t]) + off, row_bytes, width, rows,
+                            cudaMemcpyHostToDevice, hp->h2d) != cudaSuccess)
+        return SA_ERR_CUDA;
+    if (cudaEventRecord(hp->in[g], hp->h2d) != cudaSuccess) return SA_ERR_CUDA;
+  }
+  for (int g = 0; g < G; ++g) {
+    const int h0 = head0(g), h1 = head0(g + 1);
+    sa_params pg = *p;
+    pg.H = h1 - h0;
+    const size_t off = static_cast<size_t>(h0) * p->D;                 // elements
+    char* qg = static_cast<char*>(q_dev) + off * 2;
+    char* kg = static_cast<char*>(k_dev) + off * 2;
+    char* vg = static_cast<char*>(v_dev) + off * 2;
+    char* og = static_cast<char*>(o_dev) + off * 2;
+    float* lg = lse_dev ? lse_dev + static_cast<size_t>(h0) * p->S : nullptr;
+    if (cudaStreamWaitEvent(st, hp->in[g], 0) != cudaSuccess) return SA_ERR_CUDA;
+    s = sa_route(&pg, qg, kg, row_ptr, col_idx, col_cap, workspace, ws_bytes, dev_status, stream);
+    if (s != SA_OK) return s;
+    s = sa_attn_sparse(&pg, qg, kg, vg, row_ptr, col_idx, og, lg, workspace, ws_bytes,
+                       dev_status, stream);
+    if (s != SA_OK) return s;
+    if (cudaEventRecord(hp->done[g], st) != cudaSuccess ||
+        cudaStreamWaitEvent(hp->d2h, hp->done[g], 0) != cudaSuccess)
+      return SA_ERR_CUDA;
+    const size_t boff = static_cast<size_t>(h0) * p->D * 2;
+    const size_t width = static_cast<size_t>(h1 - h0) * p->D * 2;
+    if (cudaMemcpy2DAsync(static_cast<char*>(o_host) + boff, row_bytes,
+                          static_cast<const char*>(o_dev) + boff, row_bytes, width, rows,
+                          cudaMemcpyDeviceToHost, hp->d2h) != cudaSuccess)
       return SA_ERR_CUDA;
   }
+  if (lse_host && lse_dev) {
+    const size_t lb = static_cast<size_t>(p->B) * p->H * p->S * sizeof(float);
+    if (cudaMemcpyAsync(lse_host, lse_dev, lb, cudaMemcpyDeviceToHost, hp->d2h) != cudaSuccess)
+      return SA_ERR_CUDA;
+  }
+  if (cudaEventRecord(hp->end, hp->d2h) != cudaSuccess ||
+      cudaStreamWaitEvent(st, hp->end, 0) != cudaSuccess)
+    return SA_ERR_CUDA;
   return SA_OK;
 }
 

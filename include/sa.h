@@ -11,10 +11,11 @@
  *
  * Conventions shared by every entry point:
  *  - Device pointers are device memory of the current CUDA device; host
- *    pointers are named *_host. The caller owns every buffer. Apart from
- *    sa_forward_host's copies, the library never allocates, frees or
- *    synchronises: every call enqueues work on `stream` (a cudaStream_t
- *    passed as void*; NULL = the legacy default stream) and returns.
+ *    pointers are named *_host. The caller owns every buffer. The library
+ *    never allocates device memory, frees or synchronises: every call
+ *    enqueues work on `stream` (a cudaStream_t passed as void*; NULL = the
+ *    legacy default stream) and returns (sa_forward_host also uses two copy
+ *    streams of its own, see there).
  *  - The returned sa_status reports what can be checked before launch
  *    (arguments, support, launch errors). Conditions found on the device are
  *    OR-ed into *dev_status (an int32 in device memory that the caller sets
@@ -227,12 +228,21 @@ sa_status sa_attn_dense(const sa_params* p, const void* q, const void* k,
  * sa_forward_host -- one whole layer from host memory: copies q, k, v
  * (host, pinned for asynchronous copies) to the device buffers, routes,
  * attends, and copies o (and lse if both lse pointers are non-NULL) back,
- * all on `stream`, then returns without synchronising. Every device buffer
- * is the caller's, sized as for sa_route / sa_attn_sparse, with q_dev, k_dev,
- * v_dev, o_dev laid out with the strides in p and *_host contiguous copies
- * of the same [B, S, H, D] extents (the strides in p must then describe a
- * contiguous tensor). The route workspace and the attention workspace may be
- * the same buffer if it is large enough for both.
+ * then returns without synchronising. The work is split into groups of
+ * heads (up to 8 groups of at least 8 heads; one group for B > 1 with lse):
+ * each group is routed and attended as soon as its q, k, v slices have
+ * landed, and its o slice is copied back as soon as it is done, so the
+ * copies overlap the compute. Compute runs on `stream`; the copies run on two
+ * streams the library creates, with a few events, on the first call on each
+ * device and keeps until the process exits. All of it is ordered after the
+ * work enqueued on `stream` before the call and before the work enqueued on
+ * it after the call. Calls on one device from several host threads are
+ * serialised by the library. Every device buffer is the caller's, sized as
+ * for sa_route / sa_attn_sparse, with q_dev, k_dev, v_dev, o_dev laid out
+ * with the strides in p and *_host contiguous copies of the same
+ * [B, S, H, D] extents (the strides in p must then describe a contiguous
+ * tensor). The route workspace and the attention workspace may be the same
+ * buffer if it is large enough for both.
  */
 sa_status sa_forward_host(const sa_params* p, const void* q_host,
                           const void* k_host, const void* v_host, void* o_host,

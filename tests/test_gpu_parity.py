@@ -261,6 +261,27 @@ def test_forward_host_matches_device_calls(sa):
     assert np.array_equal(to_np(o_host), o_dev)
 
 
+@pytest.mark.parametrize("B,H,with_lse", [(1, 24, True), (2, 16, False), (2, 16, True)])
+def test_forward_host_head_groups_match_device_calls(sa, B, H, with_lse):
+    # H >= 16 splits the layer into head groups whose copies overlap compute;
+    # the result must be the one-call result bit for bit (the route and the
+    # tile pairing are per head)
+    S, D, P, tau = 1000, 128, 100, 1.0
+    qs, ks, vs = zip(*(sa_inputs.random_small(S, H, D, seed=40 + b) for b in range(B)))
+    q, k, v = (torch.cat(t, dim=0) for t in (qs, ks, vs))
+    bufs = sa.alloc_layer_buffers(B, S, H, D)
+    qh, kh, vh = (t.contiguous().pin_memory() for t in (q, k, v))
+    lse_host = torch.empty((B, H, S), dtype=torch.float32).pin_memory() if with_lse else None
+    o_host = sa.sa_forward_host(qh, kh, vh, P, tau, bufs=bufs, lse_host=lse_host)
+    torch.cuda.synchronize()
+    assert int(bufs["status"].item()) == 0
+    rp, ci, _ = gpu_route(sa, q, k, P, tau)
+    o_dev, lse_dev, _ = gpu_attn(sa, q, k, v, rp, ci[: rp[-1]])
+    assert np.array_equal(to_np(o_host), o_dev)
+    if with_lse:
+        assert np.array_equal(to_np(lse_host), lse_dev)
+
+
 # --------------------------------------------- release / dense / long shapes --
 
 @pytest.fixture(scope="module")

@@ -387,13 +387,20 @@ __global__ void __launch_bounds__(128) recheck_kernel(RouteArgs a) {
     const int i = static_cast<int>(row % a.Nb);
     for (int d = threadIdx.x; d < D; d += 128) qrow[d] = qb64[row * D + d];
     __syncthreads();
-    for (int k = warp; k < a.Nb; k += 4) {
-      const double* kr = kb64 + (static_cast<size_t>(bh) * a.Nb + k) * D;
-      double acc = 0.0;
-#pragma unroll
-      for (int d = lane; d < D; d += 32) acc = fma(qrow[d], kr[d], acc);
-      for (int off = 16; off >= 1; off >>= 1) acc += __shfl_xor_sync(full, acc, off);
-      if (lane == 0) s64[k] = a.scale64 * acc;
+    // one key block per thread: the fp64 unit's throughput, not shuffle
+    // latency, bounds this loop (four partial sums shorten the chains)
+    for (int k = threadIdx.x; k < a.Nb; k += 128) {
+      const double2* kr = reinterpret_cast<const double2*>(kb64 + (static_cast<size_t>(bh) * a.Nb + k) * D);
+      double acc[4] = {0.0, 0.0, 0.0, 0.0};
+#pragma unroll 8
+      for (int d2 = 0; d2 < D / 2; d2 += 2) {
+        const double2 x0 = kr[d2], x1 = kr[d2 + 1];
+        acc[0] = fma(qrow[2 * d2], x0.x, acc[0]);
+        acc[1] = fma(qrow[2 * d2 + 1], x0.y, acc[1]);
+        acc[2] = fma(qrow[2 * d2 + 2], x1.x, acc[2]);
+        acc[3] = fma(qrow[2 * d2 + 3], x1.y, acc[3]);
+      }
+      s64[k] = a.scale64 * ((acc[0] + acc[1]) + (acc[2] + acc[3]));
     }
     __syncthreads();
     double m = -INFINITY;

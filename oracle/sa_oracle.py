@@ -39,19 +39,28 @@ the docstrings below):
    log-sum-exp of the scaled logits. Non-causal. Padding tokens never enter.
 8. Dense attention = step 7 with every block kept.
 
-Two other readings of the router, selectable by ``mode`` (the pages leave the
-rule open; neither is the default):
+Other readings of the router (the pages leave the rule open; none is the
+default):
 
-* "dense_prefix_queries": step 6 as above, and every query block that
-  intersects the prefix attends every key block (a reading of "compressed
-  prefix queries" in which the prefix rows are not routed at all).
-* "top_mass": step 6 keeps, besides the sink and the diagonal, the smallest
-  set of key blocks of largest p whose summed p reaches tau (tau a mass in
-  [0, 1]): blocks are ranked by p descending, equal p by index ascending, and
-  the block of rank r is kept iff the blocks ranked above it hold less than
-  tau (MiniAcc blog, "What is Sol attention?": Sol keeps the promising pairs
-  of each head). Cumulative sums within 1e-6 of tau, and p within a relative
-  1e-6 of the last kept block's across the cut, are ties.
+* ``mode="dense_prefix_queries"``: step 6 as above, and every query block
+  that intersects the prefix attends every key block (a reading of
+  "compressed prefix queries" in which the prefix rows are not routed at all).
+* ``mode="top_mass"``: step 6 keeps, besides the sink and the diagonal, the
+  smallest set of key blocks of largest p whose summed p reaches tau (tau a
+  mass in [0, 1]): blocks are ranked by p descending, equal p by index
+  ascending, and the block of rank r is kept iff the blocks ranked above it
+  hold less than tau (MiniAcc blog, "What is Sol attention?": Sol keeps the
+  promising pairs of each head). Cumulative sums within 1e-6 of tau, and p
+  within a relative 1e-6 of the last kept block's across the cut, are ties.
+* ``q_block=128`` (non-square blocks, with any mode): query blocks of 128
+  tokens over key blocks of 64. Step 3 pools each query block over its own
+  valid tokens (up to 128), step 4 scores it against every 64-token key
+  block, step 6 compares with tau / Nb (Nb the number of key blocks) and
+  forces, besides the sink columns, the key blocks inside the query block
+  (its diagonal: key blocks 2i and 2i + 1). A query block meets the prefix
+  when 128 i < P. The route is still stated per 64-token query block: both
+  halves of a 128-token query block carry its key list, so step 7 is
+  unchanged.
 
 The parity of a Sol "correction term" for skipped pairs (MiniAcc blog, same
 section) is not pinned: the pages give no formula and it is not applied.
@@ -65,6 +74,7 @@ from typing import Dict, Iterable, List, Optional, Sequence, Tuple
 import numpy as np
 
 BLOCK = 64
+Q_BLOCKS = (64, 128)      # query block sizes of the router readings
 TIE_WINDOW = 1e-6
 
 
@@ -113,25 +123,33 @@ def pooled_softmax(s: np.ndarray) -> np.ndarray:
     return e / e.sum(axis=-1, keepdims=True)
 
 
-def forced_mask(Nb: int, prefix_len: int, block: int = BLOCK) -> np.ndarray:
-    """Step 6, forced part: [Nb, Nb] bool, sink columns and the diagonal.
+def forced_mask(Nb: int, prefix_len: int, block: int = BLOCK,
+                q_block: Optional[int] = None) -> np.ndarray:
+    """Step 6, forced part: [Nq, Nb] bool, sink columns and the diagonal.
 
     Sink blocks are the key blocks that intersect the prefix [0, P), i.e.
     j < ceil(P/64); every prefix key is then attended with its exact weight.
+    The diagonal of query block i is every key block inside it: j = i for
+    square blocks, j in {2i, 2i + 1} (those that exist) for 128-token query
+    blocks. Nq = ceil(Nb / (q_block / block)) (= Nb for square blocks).
     """
+    q_block = block if q_block is None else q_block
+    r = q_block // block
+    Nq = (Nb + r - 1) // r
     n_sink = (prefix_len + block - 1) // block
-    f = np.zeros((Nb, Nb), dtype=bool)
+    f = np.zeros((Nq, Nb), dtype=bool)
     f[:, :n_sink] = True
-    f[np.arange(Nb), np.arange(Nb)] = True
+    for i in range(Nq):
+        f[i, i * r:min(Nb, i * r + r)] = True
     return f
 
 
 def select_blocks(p: np.ndarray, tau: float, prefix_len: int,
-                  block: int = BLOCK) -> np.ndarray:
+                  block: int = BLOCK, q_block: Optional[int] = None) -> np.ndarray:
     """Step 6: kept[b,h,i,j] = p >= tau/Nb, OR sink, OR diagonal."""
     Nb = p.shape[-1]
     kept = p >= (tau / Nb)
-    return kept | forced_mask(Nb, prefix_len, block)
+    return kept | forced_mask(Nb, prefix_len, block, q_block)
 
 
 def select_top_mass(p: np.ndarray, tau: float) -> Tuple[np.ndarray, np.ndarray]:
@@ -192,39 +210,55 @@ ROUTE_MODES = ("threshold", "dense_prefix_queries", "top_mass")
 
 
 def route_ref(q, k, prefix_len: int, tau: float, scale: Optional[float] = None,
-              block: int = BLOCK, mode: str = "threshold") -> Dict[str, np.ndarray]:
+              block: int = BLOCK, mode: str = "threshold",
+              q_block: Optional[int] = None) -> Dict[str, np.ndarray]:
     """Steps 1-6: the block route of every (b, h, query block).
 
     Returns kept [B,H,Nb,Nb] bool, the CSR (row_ptr, col_idx), the pooled
     softmax p, the forced mask (broadcast to kept's shape) and ties, the
     decisions another correct router may take either way (never forced
     ones). ``mode`` picks the reading of step 6 (module docstring).
+
+    ``q_block`` (64 or 128, default the key block) is the query block size.
+    Rows stay per 64-token block: with 128-token query blocks, rows 2i and
+    2i + 1 are both the route of query block i (so are p, ratio, forced and
+    ties); "kept_q" and "p_q" hold the [B,H,Nq,Nb] values per query block.
     """
     if mode not in ROUTE_MODES:
         raise ValueError(f"unknown route mode {mode!r}")
+    q_block = block if q_block is None else int(q_block)
+    if q_block not in Q_BLOCKS or q_block % block:
+        raise ValueError(f"unsupported query block {q_block}")
+    r = q_block // block
     qf, kf = as_f64(q), as_f64(k)
     D = qf.shape[-1]
     scale = 1.0 / math.sqrt(D) if not scale else scale
-    qbar, kbar = pool_blocks(qf, block), pool_blocks(kf, block)
+    qbar, kbar = pool_blocks(qf, q_block), pool_blocks(kf, block)
     del qf, kf
-    p = pooled_softmax(pooled_logits(qbar, kbar, scale))
+    p = pooled_softmax(pooled_logits(qbar, kbar, scale))      # [B, H, Nq, Nb]
     Nb = p.shape[-1]
-    forced = np.broadcast_to(forced_mask(Nb, prefix_len, block), p.shape).copy()
+    forced = np.broadcast_to(forced_mask(Nb, prefix_len, block, q_block), p.shape).copy()
     if mode == "dense_prefix_queries":
-        n_sink = (prefix_len + block - 1) // block
-        forced[..., :n_sink, :] = True
+        n_prefix_q = (prefix_len + q_block - 1) // q_block    # query blocks meeting [0, P)
+        forced[..., :n_prefix_q, :] = True
     if mode == "top_mass":
         by_mass, ties = select_top_mass(p, tau)
         kept = by_mass | forced
         ratio = None
     else:
-        kept = select_blocks(p, tau, prefix_len, block) | forced
+        kept = select_blocks(p, tau, prefix_len, block, q_block) | forced
         ratio = threshold_ratio(p, tau)
         ties = np.abs(ratio - 1.0) <= TIE_WINDOW
     ties = ties & ~forced
+    kept_q, p_q = kept, p
+    if r > 1:                        # one row per 64-token block: repeat each query block's row
+        rows = np.arange(Nb) // r
+        kept, p, forced, ties = (x[..., rows, :] for x in (kept, p, forced, ties))
+        ratio = None if ratio is None else ratio[..., rows, :]
     row_ptr, col_idx = to_csr(kept)
     return {"kept": kept, "row_ptr": row_ptr, "col_idx": col_idx, "p": p,
-            "ratio": ratio, "forced": forced, "ties": ties, "qbar": qbar, "kbar": kbar}
+            "ratio": ratio, "forced": forced, "ties": ties, "qbar": qbar, "kbar": kbar,
+            "kept_q": kept_q, "p_q": p_q, "q_block": q_block}
 
 
 def block_density(kept: np.ndarray) -> float:

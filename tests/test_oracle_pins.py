@@ -372,3 +372,98 @@ def test_route_modes_forced_blocks_and_prefix_rows():
     assert (cover >= 0.5 - 1e-12).all()
     with pytest.raises(ValueError):
         oracle.route_ref(q, k, P, 1.0, mode="z")
+
+
+# ------------------------------------------- 128-token query blocks ------
+
+def _hand_inputs_qblock128(spec):
+    S, H, D = spec["S"], spec["H"], spec["D"]
+    q = np.zeros((1, S, H, D), np.float32)
+    q[0, 0:64, 0, 0] = 1.0
+    q[0, 64:128, 0, 0] = 3.0
+    q[0, 192:200, 0, 0] = 9.0      # query block 1: 8 tokens of 9 among 72 -> mean 1
+    _, k = _hand_inputs(spec)
+    return bf16(q), k
+
+
+def test_router_qblock128_hand_worked_fixture():
+    spec = json.load(open(os.path.join(GOLDEN, "route_hand_example_qblock128.json")))
+    q, k = _hand_inputs_qblock128(spec)
+    for case in spec["cases"]:
+        r = oracle.route_ref(q, k, case["prefix_len"], case["tau"], scale=spec["scale"],
+                             q_block=spec["q_block"])
+        rp, ci = r["row_ptr"], r["col_idx"]
+        rows = [list(ci[rp[i]:rp[i + 1]]) for i in range(len(rp) - 1)]
+        assert rows == case["rows"], (case, rows)
+
+
+def test_pool_qblock128_ragged_tail_closed_form():
+    S, H, D = 200, 1, 2
+    x = np.zeros((1, S, H, D))
+    x[0, :, 0, 0] = np.arange(S)
+    x[0, :, 0, 1] = 1.0
+    pooled = oracle.pool_blocks(x, 128)
+    assert pooled.shape == (1, 1, 2, 2)
+    assert pooled[0, 0, 0, 0] == 63.5 and pooled[0, 0, 1, 0] == 163.5   # 72-token tail
+    assert (pooled[0, 0, :, 1] == 1.0).all()
+
+
+def test_qblock128_forced_mask():
+    f = oracle.forced_mask(5, 0, q_block=128)       # 5 key blocks -> 3 query blocks
+    want = np.array([[1, 1, 0, 0, 0], [0, 0, 1, 1, 0], [0, 0, 0, 0, 1]], dtype=bool)
+    np.testing.assert_array_equal(f, want)
+    f = oracle.forced_mask(5, 65, q_block=128)      # sink blocks 0 and 1
+    assert f[:, :2].all() and f[1, 2:4].all() and f[2, 4] and not f[2, 2:4].any()
+    np.testing.assert_array_equal(oracle.forced_mask(5, 65, q_block=64), oracle.forced_mask(5, 65))
+
+
+@pytest.mark.parametrize("S", [640, 679])
+def test_qblock128_with_equal_halves_is_the_union_of_the_square_rows(S):
+    # When the two 64-token halves of every query block hold the same tokens
+    # (the second half reversed), the 128-token mean equals both 64-token
+    # means exactly, so each 128-block row must be the union of the two square
+    # rows (same thresholded set; diagonal {2i} or {2i+1}). A ragged 64-block
+    # alone in the last query block keeps its square row.
+    H, D = 2, 16
+    rng = np.random.default_rng(5)
+    qn = rng.standard_normal((1, S, H, D)).astype(np.float32)
+    for b0 in range(0, S - 127, 128):
+        qn[0, b0 + 64:b0 + 128] = qn[0, b0:b0 + 64][::-1]
+    q = bf16(qn)
+    k = bf16(rng.standard_normal((1, S, H, D)))
+    for P, tau in ((0, 1.0), (100, 0.8), (0, 1.6)):
+        sq = oracle.route_ref(q, k, P, tau)
+        r = oracle.route_ref(q, k, P, tau, q_block=128)
+        Nb = oracle.num_blocks(S)
+        for i in range(Nb):
+            pair = [j for j in (i - i % 2, i - i % 2 + 1) if j < Nb]
+            union = np.logical_or.reduce([sq["kept"][:, :, j] for j in pair])
+            np.testing.assert_array_equal(r["kept"][:, :, i], union)
+            np.testing.assert_array_equal(r["p"][:, :, i], sq["p"][:, :, pair[0]])
+        if S % 128:
+            np.testing.assert_array_equal(r["kept"][:, :, Nb - 1], sq["kept"][:, :, Nb - 1])
+
+
+def test_qblock128_route_invariants_and_modes():
+    S, P = 1000, 130
+    q, k, _ = sa_inputs.random_small(S, 2, 64, seed=3)
+    Nb = oracle.num_blocks(S)
+    r1 = oracle.route_ref(q, k, P, 1.0, q_block=128)
+    r2 = oracle.route_ref(q, k, P, 2.0, q_block=128)
+    assert r1["kept_q"].shape == (1, 2, 8, Nb) and r1["kept"].shape == (1, 2, Nb, Nb)
+    for r in (r1, r2):
+        kept = r["kept"]
+        np.testing.assert_array_equal(kept[:, :, 0::2][:, :, :Nb // 2], kept[:, :, 1::2])
+        assert kept[..., :3].all()                                 # sink columns
+        for i in range(Nb):                                        # both key blocks of the diagonal
+            assert kept[:, :, i, i - i % 2:min(Nb, i - i % 2 + 2)].all()
+        assert not (r["ties"] & r["forced"]).any()
+    assert not (r2["kept"] & ~r1["kept"]).any()                  # monotone in tau
+    assert oracle.route_ref(q, k, P, 0.0, q_block=128)["kept"].all()
+    dpq = oracle.route_ref(q, k, P, 1.0, q_block=128, mode="dense_prefix_queries")
+    assert dpq["kept"][:, :, :4].all()                           # P = 130 meets query blocks 0, 1
+    np.testing.assert_array_equal(dpq["kept"][:, :, 4:], r1["kept"][:, :, 4:])
+    top = oracle.route_ref(q, k, P, 0.5, q_block=128, mode="top_mass")
+    assert ((top["p"] * top["kept"]).sum(-1) >= 0.5 - 1e-12).all()
+    with pytest.raises(ValueError):
+        oracle.route_ref(q, k, P, 1.0, q_block=96)

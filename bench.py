@@ -1,7 +1,8 @@
 """Benchmark of one routed block-sparse attention layer on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload release|long|dense|mid|tiny] [--no-e2e] [--no-cpu]
+                    [--workload release|long|dense|mid|tiny] [--route-mode M] [--tau T]
+                    [--q-block 64|128] [--no-e2e] [--no-cpu]
 
 One step = the whole hot path on one batch of synthetic input already in
 HBM: sa_route (pool, score, select, recheck, scan, emit) then sa_attn_sparse
@@ -45,9 +46,9 @@ import sa_inputs  # noqa: E402
 METRIC = "ms/layer and effective TFLOP/s (% of GB300 bf16 peak) at S=38,247, ~18% density"
 UNIT = "TFLOP/s"
 # our kernels per step: the router (pool, score, select, recheck, scan, emit),
-# then the tile pairing (pair_rank, pair_match; only when there are more than
-# two query blocks), the V repack and the attention kernel; dense mode runs
-# just the last two
+# then the tile pairing (pair_rank, pair_match; only for 64-token query blocks
+# when there are more than two of them), the V repack and the attention
+# kernel; dense mode runs just the last two
 ROUTE_KERNELS, PAIR_KERNELS, ATTN_KERNELS = 6, 2, 2
 
 # DRAM traffic of one attention-kernel launch at the release workload, from
@@ -195,7 +196,7 @@ def run_ours(args):
 
     cfg = sa_inputs.get_config(args.workload, **({"H": args.heads} if args.heads else {}))
     tau = cfg.tau if args.tau is None else args.tau
-    mode = args.route_mode
+    mode, qblk = args.route_mode, args.q_block
     q, k, v = sa_inputs.make_qkv(cfg)
     B, S, H, D = q.shape
     qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
@@ -209,15 +210,15 @@ def run_ours(args):
         if ev is not None:
             ev[0].record(stream)
         if not dense:
-            sa.sa_route(qd, kd, cfg.P, tau, mode=mode, row_ptr=rp_buf, col_idx=ci_buf,
-                        workspace=ws, dev_status=status)
+            sa.sa_route(qd, kd, cfg.P, tau, mode=mode, q_block=qblk, row_ptr=rp_buf,
+                        col_idx=ci_buf, workspace=ws, dev_status=status)
         if ev is not None:
             ev[1].record(stream)
         if dense:
             sa.sa_attn_dense(qd, kd, vd, o=o, lse=lse, workspace=ws, dev_status=status)
         else:
             sa.sa_attn_sparse(qd, kd, vd, rp_buf, ci_buf, o=o, lse=lse, workspace=ws,
-                              dev_status=status)
+                              q_block=qblk, dev_status=status)
         if ev is not None:
             ev[2].record(stream)
 
@@ -258,13 +259,16 @@ def run_ours(args):
     peak = sustained if long_region else burst
     achieved = flops / (attn_avg * 1e-3) / 1e12
     sha = file_sha(os.path.join(ROOT, "block_sparse_attention_sa_gb300", "csrc", "attn.cu"))
+    # the counter was taken on the release workload with 64-token query blocks
+    # (and the pairing's tile list): another workload or tile list has no number
     traffic = (ATTN_TRAFFIC["bytes"]
                if ATTN_TRAFFIC["attn_cu_sha256"] and sha.startswith(ATTN_TRAFFIC["attn_cu_sha256"])
-               else None)
+               and cfg.name == "release" and H == 56 and qblk == 64 and not dense else None)
 
     e2e = None if args.no_e2e else run_e2e(sa, cfg, q, k, v, bufs, flops, args, world, dev,
-                                           stream, tau, mode)
-    per_step = ATTN_KERNELS + (0 if dense else ROUTE_KERNELS + (PAIR_KERNELS if Nb > 2 else 0))
+                                           stream, tau, mode, qblk)
+    pairing = Nb > 2 and qblk == 64
+    per_step = ATTN_KERNELS + (0 if dense else ROUTE_KERNELS + (PAIR_KERNELS if pairing else 0))
 
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
@@ -273,6 +277,7 @@ def run_ours(args):
         "data": "synthetic (seeded; stands in for the model's activations)",
         "config": {"workload": cfg.name, "B": B, "S": S, "H": H, "D": D, "prefix": cfg.P,
                    "tau": tau, "route_mode": "dense" if dense else mode, "block": 64,
+                   "q_block": qblk,
                    "density": round(density, 5),
                    "routed_tflop_per_layer": round(flops / 1e12, 4),
                    "ms_route": round(statistics.mean(route_ms), 4),
@@ -290,7 +295,7 @@ def run_ours(args):
     }
     if world == 1 and not args.no_cpu and rank == 0:
         result["cpu_baseline"] = cpu_baseline(cfg, q, k, v, flops, budget_s=15.0, tau=tau,
-                                              mode=mode)
+                                              mode=mode, q_block=qblk)
     if rank == 0:
         print(json.dumps(result), flush=True)
     if world > 1:
@@ -298,21 +303,23 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def run_e2e(sa, cfg, q, k, v, bufs, flops, args, world, dev, stream, tau, mode):
+def run_e2e(sa, cfg, q, k, v, bufs, flops, args, world, dev, stream, tau, mode, qblk):
     """The same layer through sa_forward_host: pinned host Q/K/V in, host O out,
     copies inside the timed region."""
     qh, kh, vh = (t.contiguous().pin_memory() for t in (q, k, v))
     oh = torch.empty_like(qh, pin_memory=True)
     steps = max(3, min(args.steps, 10))
     for _ in range(2):
-        sa.sa_forward_host(qh, kh, vh, cfg.P, tau, bufs=bufs, mode=mode, o_host=oh)
+        sa.sa_forward_host(qh, kh, vh, cfg.P, tau, bufs=bufs, mode=mode, q_block=qblk,
+                           o_host=oh)
     torch.cuda.synchronize()
     s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize()
     s.record(stream)
     for _ in range(steps):
-        sa.sa_forward_host(qh, kh, vh, cfg.P, tau, bufs=bufs, mode=mode, o_host=oh)
+        sa.sa_forward_host(qh, kh, vh, cfg.P, tau, bufs=bufs, mode=mode, q_block=qblk,
+                           o_host=oh)
     e.record(stream)
     torch.cuda.synchronize()
     ms = timed_max_ms(s.elapsed_time(e), steps, world, dev)
@@ -324,7 +331,8 @@ def run_e2e(sa, cfg, q, k, v, bufs, flops, args, world, dev, stream, tau, mode):
 
 # ------------------------------------------------------- the CPU oracle ----
 
-def cpu_baseline(cfg, q, k, v, flops, budget_s=15.0, seed=0, tau=None, mode="threshold"):
+def cpu_baseline(cfg, q, k, v, flops, budget_s=15.0, seed=0, tau=None, mode="threshold",
+                 q_block=64):
     """Time the oracle on a bounded sample of the layer and scale to a whole
     layer: the route of one head in full, plus as many query blocks of that
     head as fit in ``budget_s`` (at least 4), extrapolated linearly to all
@@ -338,7 +346,7 @@ def cpu_baseline(cfg, q, k, v, flops, budget_s=15.0, seed=0, tau=None, mode="thr
     qs, ks, vs = (t[:, :, h:h + 1].contiguous() for t in (q, k, v))
     t0 = time.perf_counter()
     tau = cfg.tau if tau is None else tau
-    r = oracle.route_ref(qs, ks, cfg.P, float(np.float32(tau)), mode=mode)
+    r = oracle.route_ref(qs, ks, cfg.P, float(np.float32(tau)), mode=mode, q_block=q_block)
     t_route = time.perf_counter() - t0
     order = np.random.default_rng(seed).permutation(Nb)
     t_attn, n_done = 0.0, 0
@@ -362,18 +370,19 @@ def run_reference(args):
         return
     cfg = sa_inputs.get_config(args.workload)
     tau = cfg.tau if args.tau is None else args.tau
-    mode = args.route_mode
+    mode, qblk = args.route_mode, args.q_block
     q, k, v = sa_inputs.make_qkv(cfg)
     B, S, H, D = q.shape
     import oracle
     # the layer's routed FLOPs from the oracle's own route
-    ref = oracle.route_ref(q, k, cfg.P, float(np.float32(tau)), mode=mode)
+    ref = oracle.route_ref(q, k, cfg.P, float(np.float32(tau)), mode=mode, q_block=qblk)
     flops = routed_flops(ref["row_ptr"], ref["col_idx"], B, H, S, D)
     del ref
     for w in range(args.warmup):
-        cpu_baseline(cfg, q, k, v, flops, budget_s=1.0, seed=w, tau=tau, mode=mode)
-    vals = [cpu_baseline(cfg, q, k, v, flops, budget_s=5.0, seed=100 + s, tau=tau, mode=mode)
-            for s in range(args.steps)]
+        cpu_baseline(cfg, q, k, v, flops, budget_s=1.0, seed=w, tau=tau, mode=mode,
+                     q_block=qblk)
+    vals = [cpu_baseline(cfg, q, k, v, flops, budget_s=5.0, seed=100 + s, tau=tau, mode=mode,
+                         q_block=qblk) for s in range(args.steps)]
     value = statistics.mean(c["value"] for c in vals)
     ms = flops / (value * 1e12) * 1e3
     print(json.dumps({
@@ -382,7 +391,7 @@ def run_reference(args):
         "ms_per_step": round(ms, 1), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
         "config": {"workload": cfg.name, "B": B, "S": S, "H": H, "D": D, "prefix": cfg.P,
-                   "tau": tau, "route_mode": mode},
+                   "tau": tau, "route_mode": mode, "q_block": qblk},
         "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": vals[0]["cores"],
                          "kind": "oracle", "sample": vals[-1]["sample"]},
         "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -403,6 +412,8 @@ def main():
                     choices=["threshold", "dense_prefix_queries", "top_mass"],
                     help="reading of the router rule (sa.h SA_ROUTE_*)")
     ap.add_argument("--tau", type=float, default=None, help="override the workload's tau")
+    ap.add_argument("--q-block", type=int, default=64, choices=[64, 128],
+                    help="query block of the route (128: two key blocks per query block)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     args = ap.parse_args()

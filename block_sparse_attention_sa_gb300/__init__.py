@@ -65,7 +65,7 @@ class sa_params(ctypes.Structure):
         ("tau", ctypes.c_float), ("softmax_scale", ctypes.c_float),
         ("q_stride", ctypes.c_int64 * 3), ("k_stride", ctypes.c_int64 * 3),
         ("v_stride", ctypes.c_int64 * 3), ("o_stride", ctypes.c_int64 * 3),
-        ("route_mode", ctypes.c_int32), ("reserved", ctypes.c_int32),
+        ("route_mode", ctypes.c_int32), ("q_block", ctypes.c_int32),
     ]
 
 
@@ -147,10 +147,10 @@ def _require_cuda(*ts):
 
 def make_params(q: torch.Tensor, k: Optional[torch.Tensor] = None, v: Optional[torch.Tensor] = None,
                 o: Optional[torch.Tensor] = None, prefix_len: int = 0, tau: float = 1.0,
-                scale: float = 0.0, mode="threshold") -> sa_params:
+                scale: float = 0.0, mode="threshold", q_block: int = 64) -> sa_params:
     B, S, H, D = q.shape
     p = sa_params()
-    p.B, p.S, p.H, p.D, p.block = B, S, H, D, 64
+    p.B, p.S, p.H, p.D, p.block, p.q_block = B, S, H, D, 64, int(q_block)
     p.prefix_len, p.tau, p.softmax_scale = int(prefix_len), float(tau), float(scale)
     p.route_mode = ROUTE_MODES[mode] if isinstance(mode, str) else int(mode)
     for field, t in (("q_stride", q), ("k_stride", k if k is not None else q),
@@ -183,17 +183,19 @@ def _workspace(nbytes: int, device, ws: Optional[torch.Tensor]) -> torch.Tensor:
 
 
 def sa_route(q: torch.Tensor, k: torch.Tensor, prefix_len: int, tau: float, scale: float = 0.0, *,
-             mode="threshold", row_ptr: Optional[torch.Tensor] = None,
+             mode="threshold", q_block: int = 64, row_ptr: Optional[torch.Tensor] = None,
              col_idx: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
              dev_status: Optional[torch.Tensor] = None,
              stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
     """Block route of every (b, h, query block): int32 row_ptr [B*H*Nb+1] and
     col_idx (capacity B*H*Nb*Nb unless given; valid entries are
     col_idx[:row_ptr[-1]]). ``mode``: "threshold", "dense_prefix_queries" or
-    "top_mass" (the SA_ROUTE_* readings of sa.h)."""
+    "top_mass" (the SA_ROUTE_* readings of sa.h). ``q_block``: 64, or 128 for
+    128-token query blocks (rows 2i and 2i + 1 then hold the same list)."""
     _require_cuda(q, k)
     lib = load_library()
-    p = make_params(q, k, prefix_len=prefix_len, tau=tau, scale=scale, mode=mode)
+    p = make_params(q, k, prefix_len=prefix_len, tau=tau, scale=scale, mode=mode,
+                    q_block=q_block)
     rows = int(lib.sa_route_rows(ctypes.byref(p)))
     if rows == 0:
         _check(SA_ERR_INVALID_ARG, "sa_route")
@@ -221,13 +223,15 @@ def _attn_out(q, o, lse, want_lse):
 def sa_attn_sparse(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, row_ptr: torch.Tensor,
                    col_idx: torch.Tensor, scale: float = 0.0, *, o: Optional[torch.Tensor] = None,
                    lse: Optional[torch.Tensor] = None, want_lse: bool = True,
-                   workspace: Optional[torch.Tensor] = None,
+                   workspace: Optional[torch.Tensor] = None, q_block: int = 64,
                    dev_status: Optional[torch.Tensor] = None, stream=None):
-    """Attention over the routed key blocks: (o bf16 [B,S,H,D], lse fp32 [B,H,S] or None)."""
+    """Attention over the routed key blocks: (o bf16 [B,S,H,D], lse fp32 [B,H,S] or None).
+    ``q_block`` = 128 when the route came from sa_route(..., q_block=128): the
+    kernel's tiles are then the 128-token query blocks, with no pairing step."""
     _require_cuda(q, k, v, row_ptr, col_idx)
     lib = load_library()
     o, lse = _attn_out(q, o, lse, want_lse)
-    p = make_params(q, k, v, o, scale=scale)
+    p = make_params(q, k, v, o, scale=scale, q_block=q_block)
     ws = _workspace(sa_attn_workspace_bytes(p), q.device, workspace)
     code = lib.sa_attn_sparse(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(row_ptr),
                               _ptr(col_idx), _ptr(o), _ptr(lse), _ptr(ws),
@@ -255,7 +259,7 @@ def sa_attn_dense(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: floa
 
 def sa_forward_host(q_host: torch.Tensor, k_host: torch.Tensor, v_host: torch.Tensor,
                     prefix_len: int, tau: float, scale: float = 0.0, *, bufs: dict,
-                    mode="threshold", o_host: Optional[torch.Tensor] = None,
+                    mode="threshold", q_block: int = 64, o_host: Optional[torch.Tensor] = None,
                     lse_host: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
     """One layer from (pinned) host tensors through the device buffers in
     ``bufs`` (q, k, v, o, lse, row_ptr, col_idx, ws, status); returns o_host.
@@ -263,7 +267,8 @@ def sa_forward_host(q_host: torch.Tensor, k_host: torch.Tensor, v_host: torch.Te
     lib = load_library()
     if o_host is None:
         o_host = torch.empty_like(q_host, pin_memory=True)
-    p = make_params(bufs["q"], prefix_len=prefix_len, tau=tau, scale=scale, mode=mode)
+    p = make_params(bufs["q"], prefix_len=prefix_len, tau=tau, scale=scale, mode=mode,
+                    q_block=q_block)
     ws = bufs["ws"]
     code = lib.sa_forward_host(
         ctypes.byref(p), _ptr(q_host), _ptr(k_host), _ptr(v_host), _ptr(o_host), _ptr(lse_host),

@@ -7,7 +7,11 @@
 // paragraph). The rule evaluated here: qbar/kbar = mean of the valid tokens of
 // each 64-token block; s_ij = scale * qbar_i . kbar_j over every key block;
 // p_ij = softmax_j(s_ij); keep j iff p_ij >= tau/Nb, or j is a sink block
-// (j < ceil(P/64)), or j == i.
+// (j < ceil(P/64)), or j == i. With 128-token query blocks (q_block = 128)
+// qbar_i pools query tokens [128 i, 128 i + 128), the diagonal is key blocks
+// 2i and 2i + 1, and rows 2i and 2i + 1 of the CSR both get query block i's
+// list; the kernels below index routed rows by query block (B*H*Nq of them)
+// and only scan/emit expand them to the CSR's B*H*Nb rows.
 //
 // Kernels, in launch order:
 //   pool     Q and K read once; block sums accumulated error-free (TwoSum in
@@ -53,7 +57,8 @@ __device__ __forceinline__ T* ws_ptr(char* ws, size_t off) {
 
 // ---------------------------------------------------------------- pool ---
 // grid (Nb, ceil(H*D / 1024), 2*B), 128 threads; each thread owns 8
-// consecutive d of one head (a 16-byte load per token).
+// consecutive d of one head (a 16-byte load per token). Query blocks are
+// qblk tokens long (Nq of them per head), key blocks 64.
 template <int D>
 __global__ void __launch_bounds__(128) pool_kernel(RouteArgs a) {
   const int i = blockIdx.x;
@@ -66,8 +71,11 @@ __global__ void __launch_bounds__(128) pool_kernel(RouteArgs a) {
   const int d = active ? e0 % D : 0;
   const uint16_t* X = which ? a.k : a.q;
   const int64_t* st = which ? a.ks : a.qs;
-  const int t0 = i * kBlock;
-  const int n = min(kBlock, a.S - t0);
+  const int blk = which ? kBlock : a.qblk;
+  const int nrow = which ? a.Nb : a.Nq;   // pooled rows per head
+  if (i >= nrow) return;                  // uniform over the CTA
+  const int t0 = i * blk;
+  const int n = min(blk, a.S - t0);
 
   float s[8], c[8];
 #pragma unroll
@@ -97,7 +105,7 @@ __global__ void __launch_bounds__(128) pool_kernel(RouteArgs a) {
   double sq = 0.0;
   if (active) {
     const int bh = b * a.H + h;
-    const size_t row = static_cast<size_t>(bh) * a.Nb + i;
+    const size_t row = static_cast<size_t>(bh) * nrow + i;
     float* p32 = ws_ptr<float>(a.ws, which ? a.L.kbar32 : a.L.qbar32) + row * D + d;
     double* p64 = ws_ptr<double>(a.ws, which ? a.L.kbar64 : a.L.qbar64) + row * D + d;
     double m[8];
@@ -117,7 +125,7 @@ __global__ void __launch_bounds__(128) pool_kernel(RouteArgs a) {
   for (int off = D / 16; off >= 1; off >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, off);
   if (active && d == 0) {
     const int bh = b * a.H + h;
-    const size_t row = static_cast<size_t>(bh) * a.Nb + i;
+    const size_t row = static_cast<size_t>(bh) * nrow + i;
     const float nrm = static_cast<float>(sqrt(sq) * (1.0 + 1e-6));  // rounded up
     ws_ptr<float>(a.ws, which ? a.L.knorm : a.L.qnorm)[row] = nrm;
     if (which) atomicMax(ws_ptr<int>(a.ws, a.L.kmax) + bh, __float_as_int(nrm));
@@ -125,8 +133,9 @@ __global__ void __launch_bounds__(128) pool_kernel(RouteArgs a) {
 }
 
 // --------------------------------------------------------------- score ---
-// grid (n_ct, n_ct, B*H), 256 threads; a 64x64 tile of pooled logits,
-// 4x4 outputs per thread, D consumed in chunks of 32.
+// grid (n_ct, n_qt, B*H), 256 threads; a 64x64 tile of pooled logits
+// (query blocks x key blocks), 4x4 outputs per thread, D consumed in chunks
+// of 32.
 template <int D>
 __global__ void __launch_bounds__(256) score_kernel(RouteArgs a) {
   constexpr int T = kScoreTile, KC = 32;
@@ -134,7 +143,7 @@ __global__ void __launch_bounds__(256) score_kernel(RouteArgs a) {
   __shared__ __align__(16) float Ks[KC][T];
   const int j0 = blockIdx.x * T, i0 = blockIdx.y * T, bh = blockIdx.z;
   const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
-  const float* qb = ws_ptr<float>(a.ws, a.L.qbar32) + static_cast<size_t>(bh) * a.Nb * D;
+  const float* qb = ws_ptr<float>(a.ws, a.L.qbar32) + static_cast<size_t>(bh) * a.Nq * D;
   const float* kb = ws_ptr<float>(a.ws, a.L.kbar32) + static_cast<size_t>(bh) * a.Nb * D;
 
   float acc[4][4];
@@ -146,7 +155,7 @@ __global__ void __launch_bounds__(256) score_kernel(RouteArgs a) {
   const int lr = tid >> 2, lc = (tid & 3) * 8;  // loader: row, 8 dims
   for (int d0 = 0; d0 < D; d0 += KC) {
     float4 qa = make_float4(0, 0, 0, 0), qb4 = qa, ka = qa, kb4 = qa;
-    if (i0 + lr < a.Nb) {
+    if (i0 + lr < a.Nq) {
       const float4* src = reinterpret_cast<const float4*>(qb + static_cast<size_t>(i0 + lr) * D + d0 + lc);
       qa = src[0];
       qb4 = src[1];
@@ -215,8 +224,8 @@ __global__ void __launch_bounds__(256) score_kernel(RouteArgs a) {
     }
 #pragma unroll
     for (int off = 8; off >= 1; off >>= 1) se += __shfl_xor_sync(0xffffffffu, se, off);
-    if (i < a.Nb) {
-      const size_t row = static_cast<size_t>(bh) * a.Nb + i;
+    if (i < a.Nq) {
+      const size_t row = static_cast<size_t>(bh) * a.Nq + i;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         const int j = j0 + tx * 4 + c;
@@ -230,22 +239,35 @@ __global__ void __launch_bounds__(256) score_kernel(RouteArgs a) {
   }
 }
 
+// Key block j of routed row (query block i) is forced: a sink block, or one
+// of the qr key blocks inside the query block (its diagonal).
+__device__ __forceinline__ bool forced_block(const RouteArgs& a, int i, int j) {
+  return j < a.n_sink || static_cast<unsigned>(j - i * a.qr) < static_cast<unsigned>(a.qr);
+}
+
+// The routed row (query block) whose list CSR row r (a 64-token block) holds.
+__device__ __forceinline__ int64_t routed_row(const RouteArgs& a, int64_t r) {
+  if (a.qr == 1) return r;
+  const int64_t bh = r / a.Nb;
+  return bh * a.Nq + (r - bh * a.Nb) / a.qr;
+}
+
 // -------------------------------------------------------------- select ---
-// one warp per row (b, h, i); 8 rows per 256-thread CTA.
+// one warp per routed row (b, h, query block i); 8 rows per 256-thread CTA.
 __global__ void __launch_bounds__(256) select_kernel(RouteArgs a) {
   const unsigned full = 0xffffffffu;
   const int lane = threadIdx.x & 31;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
-  if (row >= a.L.rows) return;
-  const int bh = static_cast<int>(row / a.Nb);
-  const int i = static_cast<int>(row % a.Nb);
+  if (row >= a.L.qrows) return;
+  const int bh = static_cast<int>(row / a.Nq);
+  const int i = static_cast<int>(row % a.Nq);
   uint32_t* bits = ws_ptr<uint32_t>(a.ws, a.L.bits) + row * a.words;
   int cnt = 0;
   bool flag = false;
 
   // rows that keep every key block: tau = 0 (outside top-mass), or a query
   // block meeting the prefix when prefix query rows are dense
-  const bool row_all = a.keep_all || (a.mode == SA_ROUTE_DENSE_PREFIX_QUERIES && i < a.n_sink);
+  const bool row_all = a.keep_all || (a.mode == SA_ROUTE_DENSE_PREFIX_QUERIES && i < a.n_prefix_q);
   if (row_all) {
     for (int w = 0; w < a.words; ++w) {
       const int j = w * 32 + lane;
@@ -333,7 +355,7 @@ __global__ void __launch_bounds__(256) select_kernel(RouteArgs a) {
         const int j = w * 32 + lane;
         bool keep = false;
         if (j < a.Nb) {
-          const bool forced = (j < a.n_sink) || (j == i);
+          const bool forced = forced_block(a, i, j);
           keep = forced || take_all || (!take_none && srow[j] > lo);
         }
         const uint32_t m = __ballot_sync(full, keep);
@@ -345,7 +367,7 @@ __global__ void __launch_bounds__(256) select_kernel(RouteArgs a) {
       const int j = w * 32 + lane;
       bool keep = false;
       if (j < a.Nb) {
-        const bool forced = (j < a.n_sink) || (j == i);
+        const bool forced = forced_block(a, i, j);
         const float margin = srow[j] - T;
         keep = forced || (margin >= 0.f);
         if (!forced && fabsf(margin) <= fmaf(gq, kn[j], err_row)) flag = true;
@@ -383,8 +405,8 @@ __global__ void __launch_bounds__(128) recheck_kernel(RouteArgs a) {
 
   for (int f = blockIdx.x; f < nflag; f += gridDim.x) {
     const int64_t row = ws_ptr<int>(a.ws, a.L.flags)[f];
-    const int bh = static_cast<int>(row / a.Nb);
-    const int i = static_cast<int>(row % a.Nb);
+    const int bh = static_cast<int>(row / a.Nq);
+    const int i = static_cast<int>(row % a.Nq);
     for (int d = threadIdx.x; d < D; d += 128) qrow[d] = qb64[row * D + d];
     __syncthreads();
     // one key block per thread: the fp64 unit's throughput, not shuffle
@@ -462,7 +484,7 @@ __global__ void __launch_bounds__(128) recheck_kernel(RouteArgs a) {
       const int j = w * 32 + lane;
       bool keep = false;
       if (j < a.Nb) {
-        const bool forced = (j < a.n_sink) || (j == i);
+        const bool forced = forced_block(a, i, j);
         if (a.mode == SA_ROUTE_TOP_MASS)
           keep = forced || take_all || (!take_none && s64[j] > lo);
         else
@@ -481,7 +503,8 @@ __global__ void __launch_bounds__(128) recheck_kernel(RouteArgs a) {
 }
 
 // ---------------------------------------------------------------- scan ---
-// one CTA of 1024 threads: row_ptr = exclusive scan of counts.
+// one CTA of 1024 threads: row_ptr = exclusive scan of the counts of the
+// CSR rows (each the count of its routed row).
 __global__ void __launch_bounds__(1024) scan_kernel(RouteArgs a) {
   __shared__ int64_t wsum[32];
   const int64_t n = a.L.rows;
@@ -490,7 +513,7 @@ __global__ void __launch_bounds__(1024) scan_kernel(RouteArgs a) {
   const int64_t lo = min(n, tid * per), hi = min(n, lo + per);
   const int* counts = ws_ptr<int>(a.ws, a.L.counts);
   int64_t local = 0;
-  for (int64_t r = lo; r < hi; ++r) local += counts[r];
+  for (int64_t r = lo; r < hi; ++r) local += counts[routed_row(a, r)];
   int64_t incl = local;
   for (int off = 1; off < 32; off <<= 1) {
     const int64_t v = __shfl_up_sync(0xffffffffu, incl, off);
@@ -510,19 +533,20 @@ __global__ void __launch_bounds__(1024) scan_kernel(RouteArgs a) {
   int64_t run = incl - local + (warp > 0 ? wsum[warp - 1] : 0);
   for (int64_t r = lo; r < hi; ++r) {
     a.row_ptr[r] = static_cast<int32_t>(run);
-    run += counts[r];
+    run += counts[routed_row(a, r)];
   }
   if (tid == 1023) a.row_ptr[n] = static_cast<int32_t>(wsum[31]);
 }
 
 // ---------------------------------------------------------------- emit ---
-// one warp per row: set bits of the row's mask -> ascending key blocks.
+// one warp per CSR row: set bits of its routed row's mask -> ascending key
+// blocks.
 __global__ void __launch_bounds__(256) emit_kernel(RouteArgs a) {
   const unsigned full = 0xffffffffu;
   const int lane = threadIdx.x & 31;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
   if (row >= a.L.rows) return;
-  const uint32_t* bits = ws_ptr<uint32_t>(a.ws, a.L.bits) + row * a.words;
+  const uint32_t* bits = ws_ptr<uint32_t>(a.ws, a.L.bits) + routed_row(a, row) * a.words;
   int64_t base = a.row_ptr[row];
   bool overflow = false;
   for (int w0 = 0; w0 < a.words; w0 += 32) {
@@ -560,11 +584,10 @@ cudaError_t launch_route_d(const RouteArgs& a, cudaStream_t st) {
     pool_kernel<D><<<grid, 128, 0, st>>>(a);
   }
   {
-    dim3 grid(a.n_ct, a.n_ct, a.B * a.H);
+    dim3 grid(a.n_ct, L.n_qt, a.B * a.H);
     score_kernel<D><<<grid, 256, 0, st>>>(a);
   }
-  const unsigned row_ctas = static_cast<unsigned>((L.rows + 7) / 8);
-  select_kernel<<<row_ctas, 256, 0, st>>>(a);
+  select_kernel<<<static_cast<unsigned>((L.qrows + 7) / 8), 256, 0, st>>>(a);
   {
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
@@ -578,7 +601,7 @@ cudaError_t launch_route_d(const RouteArgs& a, cudaStream_t st) {
     recheck_kernel<D><<<2 * sms, 128, smem, st>>>(a);
   }
   scan_kernel<<<1, 1024, 0, st>>>(a);
-  emit_kernel<<<row_ctas, 256, 0, st>>>(a);
+  emit_kernel<<<static_cast<unsigned>((L.rows + 7) / 8), 256, 0, st>>>(a);
   return cudaGetLastError();
 }
 
@@ -588,28 +611,33 @@ static size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255);
 
 RouteLayout route_layout(const sa_params& p) {
   RouteLayout L{};
+  const int qblk = q_block_of(p);
   L.Nb = num_blocks(p.S);
+  L.Nq = (p.S + qblk - 1) / qblk;
   L.n_ct = (L.Nb + kScoreTile - 1) / kScoreTile;
+  L.n_qt = (L.Nq + kScoreTile - 1) / kScoreTile;
   L.words = (L.Nb + 31) / 32;
   const size_t bh = static_cast<size_t>(p.B) * p.H;
   L.rows = static_cast<int64_t>(bh) * L.Nb;
-  const size_t rows = static_cast<size_t>(L.rows);
+  L.qrows = static_cast<int64_t>(bh) * L.Nq;
+  const size_t rows = static_cast<size_t>(L.rows);    // key blocks
+  const size_t qrows = static_cast<size_t>(L.qrows);  // query blocks = routed rows
   size_t off = 0;
   auto take = [&](size_t bytes) { const size_t o = off; off = align256(off + bytes); return o; };
-  L.qbar32 = take(rows * p.D * sizeof(float));
+  L.qbar32 = take(qrows * p.D * sizeof(float));
   L.kbar32 = take(rows * p.D * sizeof(float));
-  L.qbar64 = take(rows * p.D * sizeof(double));
+  L.qbar64 = take(qrows * p.D * sizeof(double));
   L.kbar64 = take(rows * p.D * sizeof(double));
-  L.qnorm = take(rows * sizeof(float));
+  L.qnorm = take(qrows * sizeof(float));
   L.knorm = take(rows * sizeof(float));
   L.kmax = take(bh * sizeof(int));
-  L.part_m = take(rows * L.n_ct * sizeof(float));
-  L.part_s = take(rows * L.n_ct * sizeof(float));
-  L.scores = take(rows * static_cast<size_t>(L.Nb) * sizeof(float));
-  L.bits = take(rows * L.words * sizeof(uint32_t));
-  L.counts = take(rows * sizeof(int));
+  L.part_m = take(qrows * L.n_ct * sizeof(float));
+  L.part_s = take(qrows * L.n_ct * sizeof(float));
+  L.scores = take(qrows * static_cast<size_t>(L.Nb) * sizeof(float));
+  L.bits = take(qrows * L.words * sizeof(uint32_t));
+  L.counts = take(qrows * sizeof(int));
   L.nflag = take(sizeof(int));
-  L.flags = take(rows * sizeof(int));
+  L.flags = take(qrows * sizeof(int));
   L.total = off;
   return L;
 }

@@ -43,8 +43,9 @@ sa_status check_params(const sa_params* p) {
   if (p->prefix_len < 0 || p->prefix_len > p->S) return SA_ERR_INVALID_ARG;
   if (!(p->tau >= 0.f) || !std::isfinite(p->tau)) return SA_ERR_INVALID_ARG;
   if (!(p->softmax_scale >= 0.f) || !std::isfinite(p->softmax_scale)) return SA_ERR_INVALID_ARG;
-  if (p->route_mode < SA_ROUTE_THRESHOLD || p->route_mode > SA_ROUTE_TOP_MASS || p->reserved != 0)
+  if (p->route_mode < SA_ROUTE_THRESHOLD || p->route_mode > SA_ROUTE_TOP_MASS)
     return SA_ERR_INVALID_ARG;
+  if (p->q_block != 0 && p->q_block != kBlock && p->q_block != 2 * kBlock) return SA_ERR_INVALID_ARG;
   if (p->route_mode == SA_ROUTE_TOP_MASS && p->tau > 1.f) return SA_ERR_INVALID_ARG;
   if (p->D != 64 && p->D != 128) return p->D > 0 ? SA_ERR_UNSUPPORTED : SA_ERR_INVALID_ARG;
   if (p->H > 65535 || p->B > 65535) return SA_ERR_UNSUPPORTED;
@@ -158,8 +159,10 @@ sa_status attn_common(const sa_params* p, const void* q, const void* k, const vo
   a.row_ptr = dense ? nullptr : row_ptr;
   a.col_idx = dense ? nullptr : col_idx;
   a.pairs = nullptr;
-  if (!dense && Nb > 2) {
-    // choose the query-block pairs of the 128-row tiles from the route
+  if (!dense && Nb > 2 && q_block_of(*p) == kBlock) {
+    // choose the query-block pairs of the 128-row tiles from the route (a
+    // route of 128-token query blocks gives both halves of each tile
+    // (2i, 2i + 1) the same list: the neighbour tiles are then exact)
     PairArgs pa{};
     pa.row_ptr = row_ptr;
     pa.col_idx = col_idx;
@@ -295,6 +298,10 @@ sa_status sa_route(const sa_params* p, const void* q, const void* k, int32_t* ro
   a.n_ct = L.n_ct;
   a.words = L.words;
   a.n_sink = (p->prefix_len + kBlock - 1) / kBlock;
+  a.qblk = q_block_of(*p);
+  a.qr = a.qblk / kBlock;
+  a.Nq = L.Nq;
+  a.n_prefix_q = (p->prefix_len + a.qblk - 1) / a.qblk;
   a.scale64 = scale64_of(p);
   a.scale = static_cast<float>(a.scale64);
   a.mode = p->route_mode;

@@ -22,8 +22,13 @@ struct RouteLayout {      // byte offsets into the caller's route workspace
   size_t qbar32, kbar32, qbar64, kbar64, qnorm, knorm, kmax;
   size_t part_m, part_s, scores, bits, counts, nflag, flags, total;
   int Nb, n_ct, words;
-  int64_t rows;
+  int Nq, n_qt;           // query blocks per head and their score tiles
+  int64_t rows;           // CSR rows, B*H*Nb (one per 64-token query block)
+  int64_t qrows;          // routed rows, B*H*Nq (one per query block)
 };
+
+// Query block size of a route: sa_params.q_block, 0 meaning 64.
+inline int q_block_of(const sa_params& p) { return p.q_block == 0 ? kBlock : p.q_block; }
 
 RouteLayout route_layout(const sa_params& p);
 
@@ -32,6 +37,8 @@ struct RouteArgs {
   const uint16_t* k;
   int64_t qs[3], ks[3];   // element strides of b, s, h
   int B, S, H, D, Nb, n_ct, words, n_sink;
+  int qblk, qr, Nq;       // query block (64 or 128), qblk / 64, query blocks per head
+  int n_prefix_q;         // query blocks meeting the prefix, ceil(P / qblk)
   float scale;            // fp32 softmax scale
   double scale64;         // fp64 softmax scale
   float log_tau_over_nb;  // logf(tau) - logf(Nb)  (tau > 0)

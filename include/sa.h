@@ -86,11 +86,12 @@ typedef struct sa_params {
   int64_t v_stride[3];
   int64_t o_stride[3];
   int32_t route_mode;     /* SA_ROUTE_*; sa_params_init sets THRESHOLD       */
-  int32_t reserved;       /* must be 0                                        */
+  int32_t q_block;        /* query block of the route: 0 or 64 (square, the
+                             default) or 128 (two key blocks); see sa_route  */
 } sa_params;
 
 /* Fills p for a contiguous [B, S, H, D] layout of all four tensors, with
- * route_mode = SA_ROUTE_THRESHOLD and softmax_scale = 0. */
+ * route_mode = SA_ROUTE_THRESHOLD, q_block = 0 and softmax_scale = 0. */
 void sa_params_init(sa_params* p, int32_t B, int32_t S, int32_t H, int32_t D,
                     int32_t prefix_len, float tau);
 
@@ -122,6 +123,13 @@ size_t sa_route_workspace_bytes(const sa_params* p);
  * first test by: rank the key blocks by p_ij descending (equal p_ij: lower j
  * first) and keep block j iff the blocks ranked above it sum to less than
  * tau.
+ * p->q_block = 128 (any mode) routes 128-token query blocks over the same
+ * 64-token key blocks: qbar_i is the mean of the valid tokens of query
+ * tokens [128 i, 128 i + 128), the threshold is still tau / Nb with Nb the
+ * number of key blocks, the diagonal of query block i is key blocks 2i and
+ * 2i + 1, and DENSE_PREFIX_QUERIES covers query blocks i < ceil(P/128). The
+ * CSR keeps one row per 64-token block: rows 2i and 2i + 1 both hold query
+ * block i's list, so sa_attn_sparse reads it unchanged.
  * Decisions match an fp64 evaluation of the rule except on ties: for
  * THRESHOLD, |p_ij * Nb / tau - 1| <= 1e-6; for TOP_MASS, a preceding mass
  * within 1e-6 of tau, or p_ij within a relative 1e-6 of the last kept
@@ -207,6 +215,12 @@ size_t sa_attn_workspace_bytes(const sa_params* p);
  * lse        device fp32 [B, H, S] (natural log), or NULL.
  * workspace  device scratch of sa_attn_workspace_bytes(p) bytes, 256-byte
  *            aligned.
+ * Each 128-row tile of the kernel holds two 64-token query blocks of one
+ * head. With p->q_block = 0 or 64 the pairs are chosen per call from the
+ * route (largest key-list overlap, among blocks at most 32 apart); with
+ * p->q_block = 128 the tiles are the 128-token query blocks (2i, 2i + 1),
+ * which share their key list when the route came from sa_route with the
+ * same q_block (any CSR is still attended exactly).
  */
 sa_status sa_attn_sparse(const sa_params* p, const void* q, const void* k,
                          const void* v, const int32_t* row_ptr,

@@ -59,7 +59,7 @@ def test_sizes(sa):
     ("D", 96, 2), ("D", 0, 1), ("block", 32, 1), ("S", 0, 1), ("prefix_len", -1, 1),
     ("prefix_len", 40000, 1), ("tau", -1.0, 1), ("tau", float("inf"), 1), ("H", 0, 1),
     ("softmax_scale", float("nan"), 1), ("route_mode", 3, 1), ("route_mode", -1, 1),
-    ("reserved", 1, 1),
+    ("q_block", 1, 1), ("q_block", 96, 1), ("q_block", 256, 1),
 ])
 def test_bad_params_rejected_before_launch(sa, field, value, code):
     L = sa.load_library()
@@ -88,6 +88,23 @@ def test_route_modes_and_their_tau_ranges(sa):
                       None, None) == 1
     p.route_mode = sa.SA_ROUTE_DENSE_PREFIX_QUERIES         # a multiple of 1/Nb: any tau >= 0
     assert L.sa_route_workspace_bytes(ctypes.byref(p)) > 0
+
+
+def test_query_block_sizes_and_route_workspace(sa):
+    L = sa.load_library()
+    p = params(sa)
+    assert p.q_block == 0                                  # what sa_params_init sets: 64
+    square = L.sa_route_workspace_bytes(ctypes.byref(p))
+    p.q_block = 64
+    assert L.sa_route_workspace_bytes(ctypes.byref(p)) == square
+    p.q_block = 128                                        # half the routed rows
+    ws128 = L.sa_route_workspace_bytes(ctypes.byref(p))
+    assert 0 < ws128 < square
+    # the CSR is still one row per 64-token block, and attention needs the same workspace
+    assert L.sa_route_rows(ctypes.byref(p)) == 56 * 598
+    assert L.sa_route_max_nnz(ctypes.byref(p)) == 56 * 598 * 598
+    p64 = params(sa)
+    assert L.sa_attn_workspace_bytes(ctypes.byref(p)) == L.sa_attn_workspace_bytes(ctypes.byref(p64))
 
 
 def test_null_and_misaligned_pointers_rejected(sa):

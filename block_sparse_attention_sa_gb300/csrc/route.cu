@@ -102,31 +102,46 @@ __global__ void __launch_bounds__(128) pool_kernel(RouteArgs a) {
     }
   }
 
-  double sq = 0.0;
+  // Block means: fp64 (s + c is the exact block sum) for the recheck, fp32
+  // for the scores. Every block but a ragged last one holds a power-of-two
+  // count, so the fp64 division is an exact scaling (one multiply) there: the
+  // fp64 unit, a small fraction of the fp32 rate on this GPU, is kept to a
+  // conversion, an add and a multiply per value.
+  float sq = 0.f;
   if (active) {
     const int bh = b * a.H + h;
     const size_t row = static_cast<size_t>(bh) * nrow + i;
     float* p32 = ws_ptr<float>(a.ws, which ? a.L.kbar32 : a.L.qbar32) + row * D + d;
     double* p64 = ws_ptr<double>(a.ws, which ? a.L.kbar64 : a.L.qbar64) + row * D + d;
+    const bool pow2 = (n & (n - 1)) == 0;
+    const double inv = 1.0 / static_cast<double>(n);    // exact for a power of two
     double m[8];
+    float m32[8];
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
-      m[u] = (static_cast<double>(s[u]) + static_cast<double>(c[u])) / static_cast<double>(n);
-      sq += m[u] * m[u];
+      const double sum = static_cast<double>(s[u]) + static_cast<double>(c[u]);
+      m[u] = pow2 ? sum * inv : sum / static_cast<double>(n);
+      // the fp32 mean: the sum rounded once to fp32, then the exact scaling
+      m32[u] = pow2 ? __fadd_rn(s[u], c[u]) * static_cast<float>(inv) : static_cast<float>(m[u]);
+      sq = fmaf(m32[u], m32[u], sq);
     }
-    reinterpret_cast<float4*>(p32)[0] = make_float4(float(m[0]), float(m[1]), float(m[2]), float(m[3]));
-    reinterpret_cast<float4*>(p32)[1] = make_float4(float(m[4]), float(m[5]), float(m[6]), float(m[7]));
+    reinterpret_cast<float4*>(p32)[0] = make_float4(m32[0], m32[1], m32[2], m32[3]);
+    reinterpret_cast<float4*>(p32)[1] = make_float4(m32[4], m32[5], m32[6], m32[7]);
 #pragma unroll
     for (int u = 0; u < 4; ++u)
       reinterpret_cast<double2*>(p64)[u] = make_double2(m[2 * u], m[2 * u + 1]);
   }
-  // 2-norm of the pooled vector: the D/8 threads of one head are adjacent lanes.
+  // 2-norm of the pooled vector (an upper bound, for the score error bound):
+  // the D/8 threads of one head are adjacent lanes. The fp32 sum of squares
+  // of the fp32 means is within a relative 16 u of the exact one (u = 2^-24;
+  // 8-term chains, a 4-level tree, the means' own rounding), its square root
+  // within 9 u; the factor 1 + 4e-6 covers that and its own rounding.
 #pragma unroll
   for (int off = D / 16; off >= 1; off >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, off);
   if (active && d == 0) {
     const int bh = b * a.H + h;
     const size_t row = static_cast<size_t>(bh) * nrow + i;
-    const float nrm = static_cast<float>(sqrt(sq) * (1.0 + 1e-6));  // rounded up
+    const float nrm = sqrtf(sq) * (1.0f + 4e-6f);
     ws_ptr<float>(a.ws, which ? a.L.knorm : a.L.qnorm)[row] = nrm;
     if (which) atomicMax(ws_ptr<int>(a.ws, a.L.kmax) + bh, __float_as_int(nrm));
   }
@@ -389,12 +404,21 @@ __global__ void __launch_bounds__(256) select_kernel(RouteArgs a) {
 }
 
 // ------------------------------------------------------------- recheck ---
-// grid-stride over the queued rows; 128 threads; fp64 throughout.
+// grid-stride over the queued rows; 256 threads (eight warps keep enough
+// independent fp64 FMA chains in flight to cover the unit's latency); fp64
+// throughout.
+constexpr int kRecheckThreads = 256, kRecheckWarps = kRecheckThreads / 32;
+static_assert(kRecheckWarps == 8, "the warp reductions below add eight partials");
+
+__device__ __forceinline__ double sum8(const double* v) {
+  return ((v[0] + v[1]) + (v[2] + v[3])) + ((v[4] + v[5]) + (v[6] + v[7]));
+}
+
 template <int D>
-__global__ void __launch_bounds__(128) recheck_kernel(RouteArgs a) {
+__global__ void __launch_bounds__(kRecheckThreads) recheck_kernel(RouteArgs a) {
   extern __shared__ __align__(16) double rs[];  // [D] qbar64 row, then [Nb] logits
-  __shared__ double red[4];
-  __shared__ int redc[4];
+  __shared__ double red[kRecheckWarps];
+  __shared__ int redc[kRecheckWarps];
   const unsigned full = 0xffffffffu;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   double* qrow = rs;
@@ -407,11 +431,11 @@ __global__ void __launch_bounds__(128) recheck_kernel(RouteArgs a) {
     const int64_t row = ws_ptr<int>(a.ws, a.L.flags)[f];
     const int bh = static_cast<int>(row / a.Nq);
     const int i = static_cast<int>(row % a.Nq);
-    for (int d = threadIdx.x; d < D; d += 128) qrow[d] = qb64[row * D + d];
+    for (int d = threadIdx.x; d < D; d += kRecheckThreads) qrow[d] = qb64[row * D + d];
     __syncthreads();
     // one key block per thread: the fp64 unit's throughput, not shuffle
     // latency, bounds this loop (four partial sums shorten the chains)
-    for (int k = threadIdx.x; k < a.Nb; k += 128) {
+    for (int k = threadIdx.x; k < a.Nb; k += kRecheckThreads) {
       const double2* kr = reinterpret_cast<const double2*>(kb64 + (static_cast<size_t>(bh) * a.Nb + k) * D);
       double acc[4] = {0.0, 0.0, 0.0, 0.0};
 #pragma unroll 8
@@ -426,25 +450,26 @@ __global__ void __launch_bounds__(128) recheck_kernel(RouteArgs a) {
     }
     __syncthreads();
     double m = -INFINITY;
-    for (int k = threadIdx.x; k < a.Nb; k += 128) m = fmax(m, s64[k]);
+    for (int k = threadIdx.x; k < a.Nb; k += kRecheckThreads) m = fmax(m, s64[k]);
     for (int off = 16; off >= 1; off >>= 1) m = fmax(m, __shfl_xor_sync(full, m, off));
     if (lane == 0) red[warp] = m;
     __syncthreads();
-    m = fmax(fmax(red[0], red[1]), fmax(red[2], red[3]));
+    m = red[0];
+    for (int w = 1; w < kRecheckWarps; ++w) m = fmax(m, red[w]);
     __syncthreads();
     double z = 0.0;
-    for (int k = threadIdx.x; k < a.Nb; k += 128) z += exp(s64[k] - m);
+    for (int k = threadIdx.x; k < a.Nb; k += kRecheckThreads) z += exp(s64[k] - m);
     for (int off = 16; off >= 1; off >>= 1) z += __shfl_xor_sync(full, z, off);
     if (lane == 0) red[warp] = z;
     __syncthreads();
-    z = (red[0] + red[1]) + (red[2] + red[3]);
+    z = sum8(red);
     __syncthreads();
     // top-mass: the same bisection as the select kernel, in fp64 on the fp64
     // softmax (blocks above lo are kept, f(lo) >= tau > f(hi))
     double lo = 0.0;
     bool take_all = false, take_none = false;
     if (a.mode == SA_ROUTE_TOP_MASS) {
-      for (int k = threadIdx.x; k < a.Nb; k += 128) s64[k] = exp(s64[k] - m) / z;
+      for (int k = threadIdx.x; k < a.Nb; k += kRecheckThreads) s64[k] = exp(s64[k] - m) / z;
       __syncthreads();
       // one warp bisects (shuffle sums only); the others wait at the barrier
       if (warp == 0) {
@@ -480,7 +505,7 @@ __global__ void __launch_bounds__(128) recheck_kernel(RouteArgs a) {
     }
     uint32_t* bits = ws_ptr<uint32_t>(a.ws, a.L.bits) + row * a.words;
     int cnt = 0;
-    for (int w = warp; w < a.words; w += 4) {
+    for (int w = warp; w < a.words; w += kRecheckWarps) {
       const int j = w * 32 + lane;
       bool keep = false;
       if (j < a.Nb) {
@@ -497,7 +522,8 @@ __global__ void __launch_bounds__(128) recheck_kernel(RouteArgs a) {
     if (lane == 0) redc[warp] = cnt;
     __syncthreads();
     if (threadIdx.x == 0)
-      ws_ptr<int>(a.ws, a.L.counts)[row] = redc[0] + redc[1] + redc[2] + redc[3];
+      ws_ptr<int>(a.ws, a.L.counts)[row] = redc[0] + redc[1] + redc[2] + redc[3] + redc[4] +
+                                           redc[5] + redc[6] + redc[7];
     __syncthreads();
   }
 }
@@ -598,7 +624,7 @@ cudaError_t launch_route_d(const RouteArgs& a, cudaStream_t st) {
                                static_cast<int>(smem));
       if (e != cudaSuccess) return e;
     }
-    recheck_kernel<D><<<2 * sms, 128, smem, st>>>(a);
+    recheck_kernel<D><<<sms, kRecheckThreads, smem, st>>>(a);
   }
   scan_kernel<<<1, 1024, 0, st>>>(a);
   emit_kernel<<<static_cast<unsigned>((L.rows + 7) / 8), 256, 0, st>>>(a);

@@ -62,6 +62,19 @@ default):
   halves of a 128-token query block carry its key list, so step 7 is
   unchanged.
 
+The step before attention (SURVEY's fused prologue; "Making MiniMax-H3 up to
+9x faster on H100s", section "Custom kernels": a fused QK-norm plus RoPE
+kernel). The page names the two operations only; the reading used here:
+
+9. QK-norm: RMS normalisation of each (token, head) vector over its D dims,
+   x_hat = x / sqrt(mean_d x_d^2 + eps) * gamma_d, with one weight vector
+   gamma [D] for Q and one for K.
+10. RoPE: each interleaved pair (2i, 2i + 1) of x_hat is rotated by the angle
+    of token t and pair i, given as tables cos[t, i], sin[t, i]:
+    (a, b) -> (a cos - b sin, a sin + b cos). 1-D and 3-D (video) rotary
+    schemes differ only in the tables.
+11. The router then pools the rounded (bf16) outputs, as in step 3.
+
 The parity of a Sol "correction term" for skipped pairs (MiniAcc blog, same
 section) is not pinned: the pages give no formula and it is not applied.
 """
@@ -377,3 +390,27 @@ def tie_mask(ratio: np.ndarray, forced: np.ndarray) -> np.ndarray:
     """Decisions another correct router may take either way: router ties
     (|p Nb / tau - 1| <= 1e-6) on blocks that are not forced."""
     return (np.abs(ratio - 1.0) <= TIE_WINDOW) & ~forced
+
+
+def qk_prologue_ref(x, gamma: Optional[np.ndarray], eps: float,
+                    cos: Optional[np.ndarray], sin: Optional[np.ndarray]) -> np.ndarray:
+    """Steps 9-10: QK-norm then RoPE of x [B, S, H, D] in fp64.
+
+    gamma [D] (None: ones), cos/sin [S, D/2] (None: no rotation). Returns the
+    exact result in fp64; the CUDA kernel rounds it once to bf16.
+    """
+    xf = as_f64(x)
+    D = xf.shape[-1]
+    ms = (xf * xf).mean(axis=-1, keepdims=True)
+    y = xf / np.sqrt(ms + eps)
+    if gamma is not None:
+        y = y * np.asarray(gamma, dtype=np.float64)
+    if cos is None:
+        return y
+    c = np.asarray(cos, dtype=np.float64)[None, :, None, :]      # [1, S, 1, D/2]
+    s_ = np.asarray(sin, dtype=np.float64)[None, :, None, :]
+    a, b = y[..., 0::2], y[..., 1::2]
+    out = np.empty_like(y)
+    out[..., 0::2] = a * c - b * s_
+    out[..., 1::2] = a * s_ + b * c
+    return out

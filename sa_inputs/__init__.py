@@ -27,6 +27,14 @@ nearby blocks. Draw order from one seeded ``torch.Generator('cpu')``: Q noise,
 K noise, V, then W. Values are drawn in fp32 and rounded once to bf16
 (round-to-nearest-even).
 
+For the QK-norm + RoPE prologue the module also draws the norm weights
+(``qk_norm_weights``: gamma = 1 + 0.1 N(0,1), one vector for Q and one for K,
+from their own seeded generator) and builds the rotary tables
+(``rope_tables``: cos/sin of the angle of every token and pair, fp32
+[S, D/2]; 1-D over the token index, or 3-D over (t, y, x) for the latent-grid
+workloads with the prefix tokens along t). These are inputs of the kernel,
+as the model's weights and positions would be.
+
 The amplitudes ``A`` and the Tiny/Long ``tau`` values are calibration results
 (bisection on the oracle's block density); the script that produced them is
 ``oracle/calibrate.py``.
@@ -190,3 +198,44 @@ def random_small(S: int, H: int, D: int, seed: int, B: int = 1, std: float = 1.0
     shape = (B, S, H, D)
     return tuple((torch.randn(shape, generator=g) * std).to(torch.bfloat16)
                  for _ in range(3))
+
+
+def qk_norm_weights(D: int, seed: int = 0) -> Tuple[torch.Tensor, torch.Tensor]:
+    """QK-norm weights gamma_q, gamma_k: fp32 [D] each, 1 + 0.1 N(0,1)."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(1000 + seed)
+    return tuple((1.0 + 0.1 * torch.randn(D, generator=g)).float() for _ in range(2))
+
+
+def rope_tables(cfg: Config, base: float = 10000.0) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Rotary tables cos, sin: fp32 [S, D/2] (pair i of token t turns by theta[t, i]).
+
+    1-D (iid, pos1d): theta = t * base^(-2i/D) over the token index t.
+    3-D (grid3d): the D/2 pairs split into t, y, x sections (the y and x
+    sections D/12 pairs each, rounded down; t the rest); within a section of
+    n pairs, pair j turns by pos * base^(-j/n), pos the token's coordinate on
+    that axis. Prefix token j sits at t = j, y = x = 0; grid token (f, y, x)
+    at t = P + f.
+    """
+    S, D = cfg.S, cfg.D
+    half = D // 2
+    if cfg.kind != "grid3d":
+        t = torch.arange(S, dtype=torch.float64)[:, None]
+        w = base ** (-2.0 * torch.arange(half, dtype=torch.float64) / D)
+        ang = t * w[None, :]
+    else:
+        _, Y, X = cfg.grid
+        n_y = n_x = D // 12
+        n_t = half - n_y - n_x
+        idx = torch.arange(S, dtype=torch.int64)
+        g = (idx - cfg.P).clamp(min=0)
+        pre = idx < cfg.P
+        tpos = torch.where(pre, idx, cfg.P + g // (Y * X)).double()
+        ypos = torch.where(pre, torch.zeros_like(idx), (g // X) % Y).double()
+        xpos = torch.where(pre, torch.zeros_like(idx), g % X).double()
+        cols = []
+        for pos, n in ((tpos, n_t), (ypos, n_y), (xpos, n_x)):
+            w = base ** (-torch.arange(n, dtype=torch.float64) / n)
+            cols.append(pos[:, None] * w[None, :])
+        ang = torch.cat(cols, dim=1)
+    return torch.cos(ang).float().contiguous(), torch.sin(ang).float().contiguous()

@@ -467,3 +467,77 @@ def test_qblock128_route_invariants_and_modes():
     assert ((top["p"] * top["kept"]).sum(-1) >= 0.5 - 1e-12).all()
     with pytest.raises(ValueError):
         oracle.route_ref(q, k, P, 1.0, q_block=96)
+
+
+# ------------------------------------------------ QK-norm + RoPE prologue --
+# The fused prologue before attention ("Making MiniMax-H3 up to 9x faster on
+# H100s", section "Custom kernels": QK-norm plus RoPE); the formulas are the
+# oracle's reading (RMS norm over D with a weight vector, then rotation of
+# interleaved pairs by tabulated angles).
+
+def test_prologue_hand_example():
+    x = np.zeros((1, 2, 1, 4))
+    x[0, 0, 0] = [3.0, 4.0, 0.0, 0.0]        # mean square 6.25 -> 1/rms = 0.4
+    x[0, 1, 0] = [0.0, 0.0, -1.0, 1.0]       # mean square 0.5
+    gamma = np.array([1.0, 2.0, 3.0, 4.0])
+    cos = np.array([[0.0, 1.0], [1.0, 0.0]])  # token 0: pair 0 turns by 90 degrees
+    sin = np.array([[1.0, 0.0], [0.0, -1.0]]) # token 1: pair 1 turns by -90 degrees
+    out = oracle.qk_prologue_ref(x, gamma, 0.0, cos, sin)
+    # token 0: y = (1.2, 3.2, 0, 0); pair 0 (a, b) -> (-b, a)
+    np.testing.assert_allclose(out[0, 0, 0], [-3.2, 1.2, 0.0, 0.0], rtol=0, atol=1e-12)
+    # token 1: y = sqrt(2) * (0, 0, -3, 4); pair 1 (a, b) -> (b, -a)
+    r2 = math.sqrt(2.0)
+    np.testing.assert_allclose(out[0, 1, 0], [0.0, 0.0, 4 * r2, 3 * r2], rtol=0, atol=1e-12)
+
+
+def test_prologue_norm_closed_forms():
+    D, eps = 8, 1e-6
+    x = np.full((1, 3, 2, D), -0.75)
+    out = oracle.qk_prologue_ref(x, None, eps, None, None)
+    np.testing.assert_allclose(out, -0.75 / math.sqrt(0.5625 + eps), rtol=1e-14)
+    rng = np.random.default_rng(0)
+    x = rng.standard_normal((1, 5, 3, 16))
+    out = oracle.qk_prologue_ref(x, None, eps, None, None)
+    ms = (x * x).mean(-1)
+    np.testing.assert_allclose((out * out).mean(-1), ms / (ms + eps), rtol=1e-12)
+    g = rng.standard_normal(16)
+    np.testing.assert_allclose(oracle.qk_prologue_ref(x, 2 * g, eps, None, None),
+                               2 * oracle.qk_prologue_ref(x, g, eps, None, None), rtol=1e-14)
+
+
+def test_prologue_rotation_matches_complex_multiplication():
+    rng = np.random.default_rng(1)
+    S, H, D = 7, 2, 8
+    x = rng.standard_normal((1, S, H, D))
+    ang = rng.uniform(-4, 4, (S, D // 2))
+    cos, sin = np.cos(ang), np.sin(ang)
+    out = oracle.qk_prologue_ref(x, None, 1e-6, cos, sin)
+    y = oracle.qk_prologue_ref(x, None, 1e-6, None, None)
+    z = (y[..., 0::2] + 1j * y[..., 1::2]) * np.exp(1j * ang)[None, :, None, :]
+    np.testing.assert_allclose(out[..., 0::2], z.real, atol=1e-12)
+    np.testing.assert_allclose(out[..., 1::2], z.imag, atol=1e-12)
+    ident = oracle.qk_prologue_ref(x, None, 1e-6, np.ones((S, D // 2)), np.zeros((S, D // 2)))
+    np.testing.assert_array_equal(ident, y)
+    # a rotation keeps each pair's length
+    np.testing.assert_allclose(np.abs(z), np.hypot(y[..., 0::2], y[..., 1::2]), rtol=1e-12)
+
+
+def test_prologue_rope_scores_depend_on_relative_position():
+    # with the 1-D table theta = t * w, q_t . k_u depends on t - u only
+    cfg = sa_inputs.get_config("tiny")
+    cos, sin = (t.double().numpy() for t in sa_inputs.rope_tables(cfg))
+    rng = np.random.default_rng(2)
+    a, b = rng.standard_normal(cfg.D), rng.standard_normal(cfg.D)
+    S = cfg.S
+
+    def score(t, u):
+        q = np.zeros((1, S, 1, cfg.D))
+        k = np.zeros((1, S, 1, cfg.D))
+        q[0, t, 0], k[0, u, 0] = a, b
+        qo = oracle.qk_prologue_ref(q, None, 1e-6, cos, sin)[0, t, 0]
+        ko = oracle.qk_prologue_ref(k, None, 1e-6, cos, sin)[0, u, 0]
+        return float(qo @ ko)
+
+    # tables are fp32, so equal up to their rounding
+    assert abs(score(10, 3) - score(200, 193)) < 1e-4 * abs(score(10, 3)) + 1e-4
+    assert abs(score(10, 3) - score(10, 40)) > 1e-3

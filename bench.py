@@ -2,7 +2,7 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload release|long|dense|mid|tiny] [--route-mode M] [--tau T]
-                    [--q-block 64|128] [--no-e2e] [--no-cpu]
+                    [--q-block 64|128] [--prologue] [--no-e2e] [--no-cpu]
 
 One step = the whole hot path on one batch of synthetic input already in
 HBM: sa_route (pool, score, select, recheck, scan, emit) then sa_attn_sparse
@@ -17,6 +17,11 @@ launched on, W untimed warm-up steps first, with a barrier and
 torch.cuda.synchronize() on both sides; for N > 1 each rank (one GPU each,
 torchrun) runs an independent replica of the layer (the path has no exchange
 step) and the max time over ranks is used.
+
+--prologue adds the QK-norm + RoPE step in front (sa_qk_prologue on the
+workload's Q, K taken as the pre-norm projections, with seeded norm weights
+and the workload's rotary tables), which also pools Q and K for the router
+(sa_route_pooled replaces sa_route's own pooling pass).
 
 --impl reference times the CPU oracle (the reference arm: no code exists to
 run for this method) on a bounded sample of the same workload and scales it
@@ -205,22 +210,37 @@ def run_ours(args):
     o, lse, rp_buf, ci_buf = bufs["o"], bufs["lse"], bufs["row_ptr"], bufs["col_idx"]
     stream = torch.cuda.current_stream(dev)
     dense = cfg.dense
+    pro = args.prologue and not dense
+    if pro:
+        gq, gk = (t.to(dev) for t in sa_inputs.qk_norm_weights(D))
+        cos, sin = (t.to(dev) for t in sa_inputs.rope_tables(cfg))
+        qn, kn = torch.empty_like(qd), torch.empty_like(kd)   # the prologue's outputs
 
     def step(ev=None):
         if ev is not None:
             ev[0].record(stream)
-        if not dense:
-            sa.sa_route(qd, kd, cfg.P, tau, mode=mode, q_block=qblk, row_ptr=rp_buf,
-                        col_idx=ci_buf, workspace=ws, dev_status=status)
+        qa, ka = qd, kd
+        if pro:
+            sa.sa_qk_prologue(qd, kd, gq, gk, 1e-6, cos, sin, q_block=qblk, q_out=qn, k_out=kn,
+                              workspace=ws, dev_status=status)
+            qa, ka = qn, kn
         if ev is not None:
             ev[1].record(stream)
-        if dense:
-            sa.sa_attn_dense(qd, kd, vd, o=o, lse=lse, workspace=ws, dev_status=status)
-        else:
-            sa.sa_attn_sparse(qd, kd, vd, rp_buf, ci_buf, o=o, lse=lse, workspace=ws,
-                              q_block=qblk, dev_status=status)
+        if pro:
+            sa.sa_route_pooled(qa, ws, cfg.P, tau, k=ka, mode=mode, q_block=qblk, row_ptr=rp_buf,
+                               col_idx=ci_buf, dev_status=status)
+        elif not dense:
+            sa.sa_route(qa, ka, cfg.P, tau, mode=mode, q_block=qblk, row_ptr=rp_buf,
+                        col_idx=ci_buf, workspace=ws, dev_status=status)
         if ev is not None:
             ev[2].record(stream)
+        if dense:
+            sa.sa_attn_dense(qa, ka, vd, o=o, lse=lse, workspace=ws, dev_status=status)
+        else:
+            sa.sa_attn_sparse(qa, ka, vd, rp_buf, ci_buf, o=o, lse=lse, workspace=ws,
+                              q_block=qblk, dev_status=status)
+        if ev is not None:
+            ev[3].record(stream)
 
     for _ in range(args.warmup):
         step()
@@ -236,7 +256,7 @@ def run_ours(args):
     flops = routed_flops(row_ptr, col_idx, B, H, S, D)
     density = float(row_ptr[-1]) / (B * H * Nb * Nb)
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize()
@@ -250,8 +270,9 @@ def run_ours(args):
     sa.check_dev_status(status, "bench")
     ms_step = timed_max_ms(start.elapsed_time(end), args.steps, world, dev)
     total_ms = ms_step * args.steps
-    route_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    attn_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    pro_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    route_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    attn_ms = [e[2].elapsed_time(e[3]) for e in evs]
     value = whole_job_tflops(flops, ms_step, world)
     attn_avg = statistics.mean(attn_ms)
     burst, sustained, _, peak_src = measured_peaks()
@@ -263,9 +284,10 @@ def run_ours(args):
     # (and the pairing's tile list): another workload or tile list has no number
     traffic = (ATTN_TRAFFIC["bytes"]
                if ATTN_TRAFFIC["attn_cu_sha256"] and sha.startswith(ATTN_TRAFFIC["attn_cu_sha256"])
-               and cfg.name == "release" and H == 56 and qblk == 64 and not dense else None)
+               and cfg.name == "release" and H == 56 and qblk == 64 and not dense and not pro
+               else None)
 
-    e2e = None if args.no_e2e else run_e2e(sa, cfg, q, k, v, bufs, flops, args, world, dev,
+    e2e = None if (args.no_e2e or pro) else run_e2e(sa, cfg, q, k, v, bufs, flops, args, world, dev,
                                            stream, tau, mode, qblk)
     pairing = Nb > 2 and qblk == 64
     per_step = ATTN_KERNELS + (0 if dense else ROUTE_KERNELS + (PAIR_KERNELS if pairing else 0))
@@ -281,6 +303,11 @@ def run_ours(args):
                    "density": round(density, 5),
                    "routed_tflop_per_layer": round(flops / 1e12, 4),
                    "ms_route": round(statistics.mean(route_ms), 4),
+                   **({"prologue": "QK-norm + RoPE, pooling fused (sa_qk_prologue)",
+                       "ms_prologue": round(statistics.mean(pro_ms), 4),
+                       # read Q, K and write them back: 4 x S x H x D x 2 bytes
+                       "prologue_gbs": round(4 * q.numel() * 2 / (statistics.mean(pro_ms) * 1e-3)
+                                             / 1e9, 1)} if pro else {}),
                    "ms_attn": round(attn_avg, 4),
                    "l2": "inputs larger than L2 (Q/K/V/O %.2f GB), no flush" % (4 * q.numel() * 2 / 1e9),
                    "parallelism": "replicas" if world > 1 else "single GPU"},
@@ -308,24 +335,32 @@ def run_e2e(sa, cfg, q, k, v, bufs, flops, args, world, dev, stream, tau, mode, 
     copies inside the timed region."""
     qh, kh, vh = (t.contiguous().pin_memory() for t in (q, k, v))
     oh = torch.empty_like(qh, pin_memory=True)
-    steps = max(3, min(args.steps, 10))
+    steps = max(5, min(args.steps, 10))
     for _ in range(2):
         sa.sa_forward_host(qh, kh, vh, cfg.P, tau, bufs=bufs, mode=mode, q_block=qblk,
                            o_host=oh)
     torch.cuda.synchronize()
-    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # each call starts after the previous one has finished (its copies back
+    # included), so an event pair per call times it exactly; the host link is
+    # shared with the machine's other GPUs, so the median call is reported
+    # (the mean beside it)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
     barrier(world)
     torch.cuda.synchronize()
-    s.record(stream)
-    for _ in range(steps):
+    for s_ev, e_ev in evs:
+        s_ev.record(stream)
         sa.sa_forward_host(qh, kh, vh, cfg.P, tau, bufs=bufs, mode=mode, q_block=qblk,
                            o_host=oh)
-    e.record(stream)
+        e_ev.record(stream)
     torch.cuda.synchronize()
-    ms = timed_max_ms(s.elapsed_time(e), steps, world, dev)
+    per = [s_ev.elapsed_time(e_ev) for s_ev, e_ev in evs]
+    ms = reduce_max(statistics.median(per), world, dev)
+    mean = reduce_max(statistics.mean(per), world, dev)
     nbytes = q.numel() * 2
     return {"value": round(whole_job_tflops(flops, ms, world), 2), "unit": UNIT,
-            "ms_per_step": round(ms, 4), "h2d_bytes_per_step": 3 * nbytes,
+            "ms_per_step": round(ms, 4), "ms_per_step_mean": round(mean, 4),
+            "timing": f"median of {steps} calls", "h2d_bytes_per_step": 3 * nbytes,
             "d2h_bytes_per_step": nbytes}
 
 
@@ -414,6 +449,8 @@ def main():
     ap.add_argument("--tau", type=float, default=None, help="override the workload's tau")
     ap.add_argument("--q-block", type=int, default=64, choices=[64, 128],
                     help="query block of the route (128: two key blocks per query block)")
+    ap.add_argument("--prologue", action="store_true",
+                    help="QK-norm + RoPE in front, with the router's pooling fused in")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     args = ap.parse_args()

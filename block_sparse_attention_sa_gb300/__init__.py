@@ -11,6 +11,8 @@ Entry points (same names as the C ABI):
     sa_route(q, k, prefix_len, tau, ...)              -> (row_ptr, col_idx)
     sa_attn_sparse(q, k, v, row_ptr, col_idx, ...)    -> (o, lse)
     sa_attn_dense(q, k, v, ...)                       -> (o, lse)
+    sa_qk_prologue(q, k, ...)                         -> (q_out, k_out, workspace)
+    sa_route_pooled(q_out, workspace, prefix_len, tau, ...) -> (row_ptr, col_idx)
     sa_forward_host(q_host, k_host, v_host, ...)      -> o_host (+ lse_host)
 Tensors are [B, S, H, D] bf16 with a contiguous last dimension.
 """
@@ -25,6 +27,7 @@ import torch
 
 __all__ = [
     "SaError", "load_library", "library_path", "sa_params", "make_params", "sa_route",
+    "sa_qk_prologue", "sa_route_pooled",
     "sa_attn_sparse", "sa_attn_dense", "sa_forward_host", "sa_route_workspace_bytes",
     "sa_attn_workspace_bytes", "sa_route_max_nnz", "check_dev_status", "EXPORTS",
     "SA_DEV_CAPACITY", "SA_DEV_TIMEOUT", "SA_DEV_BAD_ROUTE", "SA_DEV_RANGE",
@@ -47,7 +50,7 @@ EXPORTS = (
     "sa_params_init", "sa_num_blocks", "sa_route_rows", "sa_route_max_nnz",
     "sa_route_workspace_bytes", "sa_route", "sa_attn_workspace_bytes", "sa_attn_sparse",
     "sa_attn_dense", "sa_forward_host", "sa_dev_status_decode", "sa_status_string",
-    "sa_route_static",
+    "sa_route_static", "sa_qk_prologue", "sa_route_pooled",
 )
 SA_ROUTE_STATIC_WS_BYTES = 32 << 20
 
@@ -95,6 +98,9 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         "sa_attn_workspace_bytes": (sz, [P]),
         "sa_route": (ctypes.c_int, [P, vp, vp, vp, vp, i64, vp, sz, vp, vp]),
         "sa_route_static": (ctypes.c_int, [P, vp, vp, vp, vp, i64, vp, vp]),
+        "sa_qk_prologue": (ctypes.c_int, [P, vp, vp, vp, vp, ctypes.c_float, vp, vp, vp, vp, vp,
+                                          sz, vp, vp]),
+        "sa_route_pooled": (ctypes.c_int, [P, vp, vp, i64, vp, sz, vp, vp]),
         "sa_attn_sparse": (ctypes.c_int, [P, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp]),
         "sa_attn_dense": (ctypes.c_int, [P, vp, vp, vp, vp, vp, vp, sz, vp, vp]),
         "sa_forward_host": (ctypes.c_int, [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i64,
@@ -208,6 +214,61 @@ def sa_route(q: torch.Tensor, k: torch.Tensor, prefix_len: int, tau: float, scal
                         col_idx.numel(), _ptr(ws), ws.numel() * ws.element_size(),
                         _ptr(dev_status), _stream(stream))
     _check(code, "sa_route")
+    return row_ptr, col_idx
+
+
+def sa_qk_prologue(q: torch.Tensor, k: torch.Tensor, gamma_q: Optional[torch.Tensor] = None,
+                   gamma_k: Optional[torch.Tensor] = None, eps: float = 1e-6,
+                   cos: Optional[torch.Tensor] = None, sin: Optional[torch.Tensor] = None, *,
+                   q_block: int = 64, q_out: Optional[torch.Tensor] = None,
+                   k_out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                   dev_status: Optional[torch.Tensor] = None, stream=None):
+    """QK-norm + RoPE of q, k (bf16 [B,S,H,D]) with the router's pooling fused
+    in: returns (q_out, k_out, workspace); pass the workspace to
+    sa_route_pooled. gamma_* fp32 [D] or None; cos, sin fp32 [S, D/2] or None.
+    q_out/k_out default to new tensors with q/k's strides; pass q_out=q for in place."""
+    _require_cuda(q, k, gamma_q, gamma_k, cos, sin)
+    lib = load_library()
+    if q_out is None:
+        q_out = torch.empty_strided(q.shape, q.stride(), dtype=q.dtype, device=q.device)
+    if k_out is None:
+        k_out = torch.empty_strided(k.shape, k.stride(), dtype=k.dtype, device=k.device)
+    if q_out.stride() != q.stride() or k_out.stride() != k.stride():
+        raise ValueError("q_out / k_out must have the strides of q / k")
+    for t, name in ((gamma_q, "gamma_q"), (gamma_k, "gamma_k"), (cos, "cos"), (sin, "sin")):
+        if t is not None and (t.dtype != torch.float32 or not t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous fp32 tensor")
+    p = make_params(q, k, q_block=q_block)
+    ws = _workspace(sa_route_workspace_bytes(p), q.device, workspace)
+    code = lib.sa_qk_prologue(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(gamma_q), _ptr(gamma_k),
+                              float(eps), _ptr(cos), _ptr(sin), _ptr(q_out), _ptr(k_out), _ptr(ws),
+                              ws.numel() * ws.element_size(), _ptr(dev_status), _stream(stream))
+    _check(code, "sa_qk_prologue")
+    return q_out, k_out, ws
+
+
+def sa_route_pooled(q: torch.Tensor, workspace: torch.Tensor, prefix_len: int, tau: float,
+                    scale: float = 0.0, *, k: Optional[torch.Tensor] = None, mode="threshold",
+                    q_block: int = 64, row_ptr: Optional[torch.Tensor] = None,
+                    col_idx: Optional[torch.Tensor] = None,
+                    dev_status: Optional[torch.Tensor] = None, stream=None):
+    """The route from the block means sa_qk_prologue left in ``workspace``;
+    q (and k, default q's layout) give the shape and strides of that call."""
+    _require_cuda(q, workspace)
+    lib = load_library()
+    p = make_params(q, k if k is not None else q, prefix_len=prefix_len, tau=tau, scale=scale,
+                    mode=mode, q_block=q_block)
+    rows = int(lib.sa_route_rows(ctypes.byref(p)))
+    if rows == 0:
+        _check(SA_ERR_INVALID_ARG, "sa_route_pooled")
+    if row_ptr is None:
+        row_ptr = torch.empty(rows + 1, dtype=torch.int32, device=q.device)
+    if col_idx is None:
+        col_idx = torch.empty(sa_route_max_nnz(p), dtype=torch.int32, device=q.device)
+    code = lib.sa_route_pooled(ctypes.byref(p), _ptr(row_ptr), _ptr(col_idx), col_idx.numel(),
+                               _ptr(workspace), workspace.numel() * workspace.element_size(),
+                               _ptr(dev_status), _stream(stream))
+    _check(code, "sa_route_pooled")
     return row_ptr, col_idx
 
 

@@ -24,10 +24,13 @@
 //            decision inside the fp32 error bound is queued for recheck.
 //   recheck  queued rows recomputed wholly in fp64 from the fp64 pooled
 //            vectors (the same formula as the definition).
+// (prologue: QK-norm + RoPE with the pooling fused in, in place of pool, for
+// sa_qk_prologue; sa_route_pooled then runs the kernels from score on.)
 //   scan     exclusive scan of the counts -> row_ptr.
 //   emit     bitmask -> ascending col_idx, bounded by col_cap.
 #include <cfloat>
 #include <cmath>
+#include <cuda_bf16.h>
 
 #include "ptx.cuh"
 #include "sa_internal.cuh"
@@ -56,6 +59,59 @@ __device__ __forceinline__ T* ws_ptr(char* ws, size_t off) {
 }
 
 // ---------------------------------------------------------------- pool ---
+// The block sums of a thread's 8 dims (s + c exact, TwoSum) -> the fp64 and
+// fp32 block means and the vector's norm bound, in the route workspace.
+// Called by every thread of the CTA (the norm is a shuffle over the D/8
+// lanes of a head).
+template <int D>
+__device__ __forceinline__ void store_pooled(const RouteArgs& a, int which, int b, int h, int d,
+                                             int i, int nrow, int n, const float* s,
+                                             const float* c, bool active) {
+  // Block means: fp64 (s + c is the exact block sum) for the recheck, fp32
+  // for the scores. Every block but a ragged last one holds a power-of-two
+  // count, so the fp64 division is an exact scaling (one multiply) there: the
+  // fp64 unit, a small fraction of the fp32 rate on this GPU, is kept to a
+  // conversion, an add and a multiply per value.
+  float sq = 0.f;
+  if (active) {
+    const int bh = b * a.H + h;
+    const size_t row = static_cast<size_t>(bh) * nrow + i;
+    float* p32 = ws_ptr<float>(a.ws, which ? a.L.kbar32 : a.L.qbar32) + row * D + d;
+    double* p64 = ws_ptr<double>(a.ws, which ? a.L.kbar64 : a.L.qbar64) + row * D + d;
+    const bool pow2 = (n & (n - 1)) == 0;
+    const double inv = 1.0 / static_cast<double>(n);    // exact for a power of two
+    double m[8];
+    float m32[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const double sum = static_cast<double>(s[u]) + static_cast<double>(c[u]);
+      m[u] = pow2 ? sum * inv : sum / static_cast<double>(n);
+      // the fp32 mean: the sum rounded once to fp32, then the exact scaling
+      m32[u] = pow2 ? __fadd_rn(s[u], c[u]) * static_cast<float>(inv) : static_cast<float>(m[u]);
+      sq = fmaf(m32[u], m32[u], sq);
+    }
+    reinterpret_cast<float4*>(p32)[0] = make_float4(m32[0], m32[1], m32[2], m32[3]);
+    reinterpret_cast<float4*>(p32)[1] = make_float4(m32[4], m32[5], m32[6], m32[7]);
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      reinterpret_cast<double2*>(p64)[u] = make_double2(m[2 * u], m[2 * u + 1]);
+  }
+  // 2-norm of the pooled vector (an upper bound, for the score error bound):
+  // the D/8 threads of one head are adjacent lanes. The fp32 sum of squares
+  // of the fp32 means is within a relative 16 u of the exact one (u = 2^-24;
+  // 8-term chains, a 4-level tree, the means' own rounding), its square root
+  // within 9 u; the factor 1 + 4e-6 covers that and its own rounding.
+#pragma unroll
+  for (int off = D / 16; off >= 1; off >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, off);
+  if (active && d == 0) {
+    const int bh = b * a.H + h;
+    const size_t row = static_cast<size_t>(bh) * nrow + i;
+    const float nrm = sqrtf(sq) * (1.0f + 4e-6f);
+    ws_ptr<float>(a.ws, which ? a.L.knorm : a.L.qnorm)[row] = nrm;
+    if (which) atomicMax(ws_ptr<int>(a.ws, a.L.kmax) + bh, __float_as_int(nrm));
+  }
+}
+
 // grid (Nb, ceil(H*D / 1024), 2*B), 128 threads; each thread owns 8
 // consecutive d of one head (a 16-byte load per token). Query blocks are
 // qblk tokens long (Nq of them per head), key blocks 64.
@@ -101,50 +157,130 @@ __global__ void __launch_bounds__(128) pool_kernel(RouteArgs a) {
       }
     }
   }
+  store_pooled<D>(a, which, b, h, d, i, nrow, n, s, c, active);
+}
 
-  // Block means: fp64 (s + c is the exact block sum) for the recheck, fp32
-  // for the scores. Every block but a ragged last one holds a power-of-two
-  // count, so the fp64 division is an exact scaling (one multiply) there: the
-  // fp64 unit, a small fraction of the fp32 rate on this GPU, is kept to a
-  // conversion, an add and a multiply per value.
-  float sq = 0.f;
-  if (active) {
-    const int bh = b * a.H + h;
-    const size_t row = static_cast<size_t>(bh) * nrow + i;
-    float* p32 = ws_ptr<float>(a.ws, which ? a.L.kbar32 : a.L.qbar32) + row * D + d;
-    double* p64 = ws_ptr<double>(a.ws, which ? a.L.kbar64 : a.L.qbar64) + row * D + d;
-    const bool pow2 = (n & (n - 1)) == 0;
-    const double inv = 1.0 / static_cast<double>(n);    // exact for a power of two
-    double m[8];
-    float m32[8];
+// ------------------------------------------------------------ prologue ---
+// QK-norm + RoPE with the pooling fused in ("Making MiniMax-H3 up to 9x
+// faster on H100s", section "Custom kernels": a fused QK-norm plus RoPE
+// kernel). For each token of a (b, h) head vector x [D]:
+//   y_d = x_d / sqrt(mean(x^2) + eps) * gamma_d
+//   (y_2i, y_2i+1) -> (y_2i cos - y_2i+1 sin, y_2i sin + y_2i+1 cos), angle of
+//   (token, pair i) from the caller's tables
+// rounded once to bf16 and stored; the rounded values are summed per block
+// exactly as pool_kernel sums what it reads, so the pooled means are those
+// sa_route would compute from the outputs, and Q and K are not read again.
+// Same grid and thread layout as pool_kernel; plain loads (the outputs may
+// overwrite the inputs in place).
+template <int D>
+__global__ void __launch_bounds__(128) prologue_kernel(RouteArgs a, PrologueArgs pa) {
+  constexpr int kLanes = D / 8;       // threads of one head vector
+  constexpr int kChunk = 64;          // tokens whose rotary rows are staged at once
+  constexpr int kT = 8;               // tokens in flight per thread
+  // this chunk's rotary rows, [token][pair]: cos, then sin
+  __shared__ __align__(16) float tab[2][kChunk][D / 2];
+  const int i = blockIdx.x;
+  const int which = blockIdx.z & 1;  // 0: Q, 1: K
+  const int b = blockIdx.z >> 1;
+  const int e0 = (blockIdx.y * 128 + threadIdx.x) * 8;
+  const int HD = a.H * D;
+  const bool active = e0 < HD;
+  const int h = active ? e0 / D : 0;
+  const int d = active ? e0 % D : 0;
+  const uint16_t* X = which ? a.k : a.q;
+  uint16_t* Y = which ? pa.k_out : pa.q_out;
+  const int64_t* st = which ? a.ks : a.qs;
+  const float* gamma = which ? pa.gamma_k : pa.gamma_q;
+  const int blk = which ? kBlock : a.qblk;
+  const int nrow = which ? a.Nb : a.Nq;
+  if (i >= nrow) return;                  // uniform over the CTA
+  const int t0 = i * blk;
+  const int n = min(blk, a.S - t0);
+  const float inv_d = 1.0f / static_cast<float>(D);   // exact: D is a power of two
+  const bool rope = pa.cos != nullptr;
+
+  float g[8];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const double sum = static_cast<double>(s[u]) + static_cast<double>(c[u]);
-      m[u] = pow2 ? sum * inv : sum / static_cast<double>(n);
-      // the fp32 mean: the sum rounded once to fp32, then the exact scaling
-      m32[u] = pow2 ? __fadd_rn(s[u], c[u]) * static_cast<float>(inv) : static_cast<float>(m[u]);
-      sq = fmaf(m32[u], m32[u], sq);
+  for (int u = 0; u < 8; ++u) g[u] = 1.f;
+  if (active && gamma) {
+    const float4 g0 = reinterpret_cast<const float4*>(gamma + d)[0];
+    const float4 g1 = reinterpret_cast<const float4*>(gamma + d)[1];
+    g[0] = g0.x; g[1] = g0.y; g[2] = g0.z; g[3] = g0.w;
+    g[4] = g1.x; g[5] = g1.y; g[6] = g1.z; g[7] = g1.w;
+  }
+  float s[8], c[8];
+#pragma unroll
+  for (int u = 0; u < 8; ++u) s[u] = c[u] = 0.f;
+
+  const int64_t off = b * st[0] + h * st[2] + d;
+  for (int c0 = 0; c0 < n; c0 += kChunk) {
+    const int nc = min(kChunk, n - c0);
+    if (rope) {
+      // stage the chunk's rotary rows (shared by every head of the CTA)
+      __syncthreads();                    // the previous chunk's rows are read
+      constexpr int kRow4 = D / 8;        // float4 per table row
+      const float4* cs4 = reinterpret_cast<const float4*>(pa.cos) +
+                          static_cast<size_t>(t0 + c0) * kRow4;
+      const float4* sn4 = reinterpret_cast<const float4*>(pa.sin) +
+                          static_cast<size_t>(t0 + c0) * kRow4;
+      for (int e = threadIdx.x; e < nc * kRow4; e += 128) {
+        reinterpret_cast<float4*>(&tab[0][0][0])[e] = cs4[e];
+        reinterpret_cast<float4*>(&tab[1][0][0])[e] = sn4[e];
+      }
+      __syncthreads();
     }
-    reinterpret_cast<float4*>(p32)[0] = make_float4(m32[0], m32[1], m32[2], m32[3]);
-    reinterpret_cast<float4*>(p32)[1] = make_float4(m32[4], m32[5], m32[6], m32[7]);
+    for (int t = 0; t < nc; t += kT) {
+      uint4 xb[kT];
 #pragma unroll
-    for (int u = 0; u < 4; ++u)
-      reinterpret_cast<double2*>(p64)[u] = make_double2(m[2 * u], m[2 * u + 1]);
-  }
-  // 2-norm of the pooled vector (an upper bound, for the score error bound):
-  // the D/8 threads of one head are adjacent lanes. The fp32 sum of squares
-  // of the fp32 means is within a relative 16 u of the exact one (u = 2^-24;
-  // 8-term chains, a 4-level tree, the means' own rounding), its square root
-  // within 9 u; the factor 1 + 4e-6 covers that and its own rounding.
+      for (int u = 0; u < kT; ++u)
+        xb[u] = (active && t + u < nc)
+                    ? *reinterpret_cast<const uint4*>(X + off + (t0 + c0 + t + u) * st[1])
+                    : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-  for (int off = D / 16; off >= 1; off >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, off);
-  if (active && d == 0) {
-    const int bh = b * a.H + h;
-    const size_t row = static_cast<size_t>(bh) * nrow + i;
-    const float nrm = sqrtf(sq) * (1.0f + 4e-6f);
-    ws_ptr<float>(a.ws, which ? a.L.knorm : a.L.qnorm)[row] = nrm;
-    if (which) atomicMax(ws_ptr<int>(a.ws, a.L.kmax) + bh, __float_as_int(nrm));
+      for (int u = 0; u < kT; ++u) {
+        const uint32_t w[4] = {xb[u].x, xb[u].y, xb[u].z, xb[u].w};
+        float x[8];
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          x[2 * v] = bf16_to_f32(static_cast<uint16_t>(w[v] & 0xffffu));
+          x[2 * v + 1] = bf16_to_f32(static_cast<uint16_t>(w[v] >> 16));
+        }
+        float ss = 0.f;
+#pragma unroll
+        for (int v = 0; v < 8; ++v) ss = fmaf(x[v], x[v], ss);
+#pragma unroll
+        for (int o = kLanes / 2; o >= 1; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        const float r = rsqrtf(ss * inv_d + pa.eps);
+        float cv[4] = {1.f, 1.f, 1.f, 1.f}, sv[4] = {0.f, 0.f, 0.f, 0.f};
+        if (rope && t + u < nc) {
+          const float4 c4 = *reinterpret_cast<const float4*>(&tab[0][t + u][d / 2]);
+          const float4 s4 = *reinterpret_cast<const float4*>(&tab[1][t + u][d / 2]);
+          cv[0] = c4.x; cv[1] = c4.y; cv[2] = c4.z; cv[3] = c4.w;
+          sv[0] = s4.x; sv[1] = s4.y; sv[2] = s4.z; sv[3] = s4.w;
+        }
+        uint32_t packed[4];
+        float yr[8];
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          const float y0 = x[2 * v] * r * g[2 * v];
+          const float y1 = x[2 * v + 1] * r * g[2 * v + 1];
+          const float o0 = fmaf(y0, cv[v], -y1 * sv[v]);
+          const float o1 = fmaf(y0, sv[v], y1 * cv[v]);
+          const __nv_bfloat162 hb = __floats2bfloat162_rn(o0, o1);
+          packed[v] = *reinterpret_cast<const uint32_t*>(&hb);
+          yr[2 * v] = bf16_to_f32(static_cast<uint16_t>(packed[v] & 0xffffu));
+          yr[2 * v + 1] = bf16_to_f32(static_cast<uint16_t>(packed[v] >> 16));
+        }
+        if (active && t + u < nc) {
+          *reinterpret_cast<uint4*>(Y + off + (t0 + c0 + t + u) * st[1]) =
+              make_uint4(packed[0], packed[1], packed[2], packed[3]);
+#pragma unroll
+          for (int v = 0; v < 8; ++v) two_sum(s[v], c[v], yr[v]);
+        }
+      }
+    }
   }
+  store_pooled<D>(a, which, b, h, d, i, nrow, n, s, c, active);
 }
 
 // --------------------------------------------------------------- score ---
@@ -598,17 +734,12 @@ __global__ void __launch_bounds__(256) emit_kernel(RouteArgs a) {
     atomicOr(a.dev_status, SA_DEV_CAPACITY);
 }
 
+// The router after pooling: logits, selection, recheck, CSR.
 template <int D>
-cudaError_t launch_route_d(const RouteArgs& a, cudaStream_t st) {
+cudaError_t launch_select_d(const RouteArgs& a, cudaStream_t st) {
   const RouteLayout& L = a.L;
   cudaError_t e = cudaMemsetAsync(a.ws + L.nflag, 0, sizeof(int), st);
   if (e != cudaSuccess) return e;
-  e = cudaMemsetAsync(a.ws + L.kmax, 0, sizeof(int) * static_cast<size_t>(a.B) * a.H, st);
-  if (e != cudaSuccess) return e;
-  {
-    dim3 grid(a.Nb, (a.H * D + 1023) / 1024, 2 * a.B);
-    pool_kernel<D><<<grid, 128, 0, st>>>(a);
-  }
   {
     dim3 grid(a.n_ct, L.n_qt, a.B * a.H);
     score_kernel<D><<<grid, 256, 0, st>>>(a);
@@ -631,6 +762,19 @@ cudaError_t launch_route_d(const RouteArgs& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+// Pooling (pa == nullptr: pool_kernel reads q, k) or the fused prologue.
+template <int D>
+cudaError_t launch_pool_d(const RouteArgs& a, const PrologueArgs* pa, cudaStream_t st) {
+  const cudaError_t e =
+      cudaMemsetAsync(a.ws + a.L.kmax, 0, sizeof(int) * static_cast<size_t>(a.B) * a.H, st);
+  if (e != cudaSuccess) return e;
+  dim3 grid(a.Nb, (a.H * D + 1023) / 1024, 2 * a.B);
+  if (pa)
+    prologue_kernel<D><<<grid, 128, 0, st>>>(a, *pa);
+  else
+    pool_kernel<D><<<grid, 128, 0, st>>>(a);
+  return cudaGetLastError();
+}
 }  // namespace
 
 static size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -669,7 +813,16 @@ RouteLayout route_layout(const sa_params& p) {
 }
 
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t st) {
-  return a.D == 128 ? launch_route_d<128>(a, st) : launch_route_d<64>(a, st);
+  const cudaError_t e = launch_pool(a, nullptr, st);
+  return e == cudaSuccess ? launch_route_select(a, st) : e;
+}
+
+cudaError_t launch_pool(const RouteArgs& a, const PrologueArgs* pa, cudaStream_t st) {
+  return a.D == 128 ? launch_pool_d<128>(a, pa, st) : launch_pool_d<64>(a, pa, st);
+}
+
+cudaError_t launch_route_select(const RouteArgs& a, cudaStream_t st) {
+  return a.D == 128 ? launch_select_d<128>(a, st) : launch_select_d<64>(a, st);
 }
 
 }  // namespace sa

@@ -271,13 +271,19 @@ size_t sa_attn_workspace_bytes(const sa_params* p) {
   return attn_ws_bytes(p);
 }
 
-sa_status sa_route(const sa_params* p, const void* q, const void* k, int32_t* row_ptr,
-                   int32_t* col_idx, int64_t col_cap, void* workspace, size_t ws_bytes,
-                   int32_t* dev_status, void* stream) {
+}  // extern "C"
+
+namespace sa {
+namespace {
+
+// The router's launch arguments for p on the caller's workspace; q, k,
+// row_ptr, col_idx are checked by the callers that use them.
+sa_status route_args(const sa_params* p, const void* q, const void* k, int32_t* row_ptr,
+                     int32_t* col_idx, int64_t col_cap, void* workspace, size_t ws_bytes,
+                     int32_t* dev_status, RouteArgs* out) {
   sa_status s = check_params(p);
   if (s != SA_OK) return s;
-  if (!q || !k || !row_ptr || !col_idx || !workspace || col_cap < 0) return SA_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k)) return SA_ERR_INVALID_ARG;
+  if (!workspace || col_cap < 0) return SA_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return SA_ERR_INVALID_ARG;
   if (!strides_ok(p->q_stride) || !strides_ok(p->k_stride)) return SA_ERR_INVALID_ARG;
   const RouteLayout L = route_layout(*p);
@@ -324,7 +330,62 @@ sa_status sa_route(const sa_params* p, const void* q, const void* k, int32_t* ro
   a.col_idx = col_idx;
   a.col_cap = col_cap;
   a.dev_status = dev_status;
+  *out = a;
+  return SA_OK;
+}
+
+}  // namespace
+}  // namespace sa
+
+extern "C" {
+
+sa_status sa_route(const sa_params* p, const void* q, const void* k, int32_t* row_ptr,
+                   int32_t* col_idx, int64_t col_cap, void* workspace, size_t ws_bytes,
+                   int32_t* dev_status, void* stream) {
+  RouteArgs a;
+  const sa_status s = route_args(p, q, k, row_ptr, col_idx, col_cap, workspace, ws_bytes,
+                                 dev_status, &a);
+  if (s != SA_OK) return s;
+  if (!q || !k || !row_ptr || !col_idx) return SA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k)) return SA_ERR_INVALID_ARG;
   return from_cuda(launch_route(a, static_cast<cudaStream_t>(stream)));
+}
+
+sa_status sa_qk_prologue(const sa_params* p, const void* q_in, const void* k_in,
+                         const float* gamma_q, const float* gamma_k, float eps,
+                         const float* rope_cos, const float* rope_sin, void* q_out, void* k_out,
+                         void* workspace, size_t ws_bytes, int32_t* dev_status, void* stream) {
+  RouteArgs a;
+  const sa_status s = route_args(p, q_in, k_in, nullptr, nullptr, 0, workspace, ws_bytes,
+                                 dev_status, &a);
+  if (s != SA_OK) return s;
+  if (!q_in || !k_in || !q_out || !k_out) return SA_ERR_INVALID_ARG;
+  if (!aligned16(q_in) || !aligned16(k_in) || !aligned16(q_out) || !aligned16(k_out))
+    return SA_ERR_INVALID_ARG;
+  if ((gamma_q && !aligned16(gamma_q)) || (gamma_k && !aligned16(gamma_k))) return SA_ERR_INVALID_ARG;
+  if ((rope_cos == nullptr) != (rope_sin == nullptr)) return SA_ERR_INVALID_ARG;
+  if (rope_cos && (!aligned16(rope_cos) || !aligned16(rope_sin))) return SA_ERR_INVALID_ARG;
+  if (!(eps >= 0.f) || !std::isfinite(eps)) return SA_ERR_INVALID_ARG;
+  PrologueArgs pa{};
+  pa.gamma_q = gamma_q;
+  pa.gamma_k = gamma_k;
+  pa.cos = rope_cos;
+  pa.sin = rope_sin;
+  pa.eps = eps;
+  pa.q_out = static_cast<uint16_t*>(q_out);
+  pa.k_out = static_cast<uint16_t*>(k_out);
+  return from_cuda(launch_pool(a, &pa, static_cast<cudaStream_t>(stream)));
+}
+
+sa_status sa_route_pooled(const sa_params* p, int32_t* row_ptr, int32_t* col_idx,
+                          int64_t col_cap, void* workspace, size_t ws_bytes, int32_t* dev_status,
+                          void* stream) {
+  RouteArgs a;
+  const sa_status s = route_args(p, nullptr, nullptr, row_ptr, col_idx, col_cap, workspace,
+                                 ws_bytes, dev_status, &a);
+  if (s != SA_OK) return s;
+  if (!row_ptr || !col_idx) return SA_ERR_INVALID_ARG;
+  return from_cuda(launch_route_select(a, static_cast<cudaStream_t>(stream)));
 }
 
 sa_status sa_attn_sparse(const sa_params* p, const void* q, const void* k, const void* v,

@@ -56,7 +56,21 @@ struct RouteArgs {
   int32_t* dev_status;
 };
 
-cudaError_t launch_route(const RouteArgs& a, cudaStream_t st);
+// QK-norm + RoPE prologue (sa_qk_prologue): reads RouteArgs::q, k.
+struct PrologueArgs {
+  const float* gamma_q;    // [D] or nullptr (ones)
+  const float* gamma_k;
+  const float* cos;        // [S][D/2] or nullptr (no rotation; then sin too)
+  const float* sin;
+  float eps;
+  uint16_t* q_out;         // bf16 bits, strides of q (may equal q)
+  uint16_t* k_out;         // strides of k (may equal k)
+};
+
+cudaError_t launch_route(const RouteArgs& a, cudaStream_t st);   // pool + select
+// pa == nullptr: pool q, k; else the prologue writes q_out, k_out and pools them
+cudaError_t launch_pool(const RouteArgs& a, const PrologueArgs* pa, cudaStream_t st);
+cudaError_t launch_route_select(const RouteArgs& a, cudaStream_t st);
 
 // ---------------------------------------------------------- attention ---
 

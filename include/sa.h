@@ -189,6 +189,53 @@ sa_status sa_route_static(const sa_params* p, const void* q, const void* k,
                           int32_t* row_ptr, int32_t* col_idx, int64_t col_cap,
                           int32_t* dev_status, void* stream);
 
+/*
+ * sa_qk_prologue -- QK-norm + RoPE of q and k with the router's pooling
+ * fused in (the fused QK-norm plus RoPE kernel of "Making MiniMax-H3 up to
+ * 9x faster on H100s", section "Custom kernels"; the formulas are this
+ * library's reading of that step). For every (b, token t, h) vector x [D]
+ * of q_in (weights gamma_q) and of k_in (weights gamma_k):
+ *   y_d = x_d / sqrt(mean_d(x_d^2) + eps) * gamma_d
+ *   (y_2i, y_2i+1) -> (y_2i c - y_2i+1 s, y_2i s + y_2i+1 c),
+ *       c = rope_cos[t][i], s = rope_sin[t][i]
+ * computed in fp32 and rounded once to bf16 into q_out / k_out. The block
+ * means of those bf16 outputs are written into `workspace` exactly as
+ * sa_route would compute them from q_out, k_out; sa_route_pooled then
+ * routes from them, so q_out and k_out are not read again for routing.
+ *
+ * q_in, k_in   device bf16 [B, S, H, D], strides p->q_stride / p->k_stride.
+ * q_out, k_out device bf16, the same strides as q_in / k_in; each may be
+ *              the same buffer as its input (in place) but must not
+ *              otherwise overlap it.
+ * gamma_q,     device fp32 [D], 16-byte aligned, or NULL for all ones.
+ * gamma_k
+ * eps          >= 0, added to the mean square.
+ * rope_cos,    device fp32 [S][D/2] (row t = token t of the packed
+ * rope_sin     sequence, any 1-D or 3-D rotary scheme), 16-byte aligned;
+ *              both NULL for no rotation.
+ * workspace    the route workspace, sa_route_workspace_bytes(p) bytes,
+ *              256-byte aligned; p->q_block sets the query pooling.
+ * Errors: as sa_route (SA_ERR_INVALID_ARG also for a bad eps, an unaligned
+ * weight or table, or only one of the two tables).
+ */
+sa_status sa_qk_prologue(const sa_params* p, const void* q_in, const void* k_in,
+                         const float* gamma_q, const float* gamma_k, float eps,
+                         const float* rope_cos, const float* rope_sin, void* q_out,
+                         void* k_out, void* workspace, size_t ws_bytes,
+                         int32_t* dev_status, void* stream);
+
+/*
+ * sa_route_pooled -- sa_route from the block means that sa_qk_prologue left
+ * in `workspace` (steps after pooling: logits, selection, fp64 recheck,
+ * CSR). p must give the same B, S, H, D, q_block and strides as that
+ * sa_qk_prologue call (prefix_len, tau, route_mode and softmax_scale may
+ * differ); the workspace's contents are not checked. The result equals
+ * sa_route on the prologue's q_out, k_out. Arguments and errors as sa_route.
+ */
+sa_status sa_route_pooled(const sa_params* p, int32_t* row_ptr, int32_t* col_idx,
+                          int64_t col_cap, void* workspace, size_t ws_bytes,
+                          int32_t* dev_status, void* stream);
+
 /* Bytes of device workspace sa_attn_sparse / sa_attn_dense need. */
 size_t sa_attn_workspace_bytes(const sa_params* p);
 

@@ -158,3 +158,34 @@ def test_binding_refuses_cpu_tensors(sa):
         sa.sa_route(q, q, 0, 1.0)
     with pytest.raises(ValueError):
         sa.sa_attn_dense(q, q, q)
+
+
+def test_prologue_and_pooled_route_reject_bad_arguments(sa):
+    L = sa.load_library()
+    p = params(sa)
+    a = ctypes.c_void_p(4096)
+    f = ctypes.c_void_p(8192)
+    big = 1 << 40
+
+    def pro(**kw):
+        args = dict(qi=a, ki=a, gq=None, gk=None, eps=1e-6, cs=None, sn=None, qo=a, ko=a,
+                    ws=a, wsb=big)
+        args.update(kw)
+        return L.sa_qk_prologue(ctypes.byref(p), args["qi"], args["ki"], args["gq"], args["gk"],
+                                args["eps"], args["cs"], args["sn"], args["qo"], args["ko"],
+                                args["ws"], args["wsb"], None, None)
+
+    assert pro(eps=-1.0) == 1
+    assert pro(eps=float("nan")) == 1
+    assert pro(cs=f) == 1                                # one table without the other
+    assert pro(cs=f, sn=ctypes.c_void_p(8192 + 4)) == 1  # misaligned table
+    assert pro(gq=ctypes.c_void_p(8192 + 8)) == 1        # misaligned weights
+    assert pro(qo=None) == 1
+    assert pro(ki=ctypes.c_void_p(4096 + 2)) == 1
+    assert pro(ws=ctypes.c_void_p(4096 + 16)) == 1       # workspace not 256-byte aligned
+    assert pro(wsb=1024) == 3                            # workspace too small
+    assert L.sa_route_pooled(ctypes.byref(p), None, a, 10, a, big, None, None) == 1
+    assert L.sa_route_pooled(ctypes.byref(p), a, a, 10, a, 1024, None, None) == 3
+    p.D = 96
+    assert pro() == 2
+    assert L.sa_route_pooled(ctypes.byref(p), a, a, 10, a, big, None, None) == 2

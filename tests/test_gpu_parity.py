@@ -261,7 +261,7 @@ def test_forward_host_matches_device_calls(sa):
     assert np.array_equal(to_np(o_host), o_dev)
 
 
-@pytest.mark.parametrize("B,H,with_lse", [(1, 24, True), (2, 16, False), (2, 16, True)])
+@pytest.mark.parametrize("B,H,with_lse", [(1, 24, True), (2, 16, False), (2, 16, True), (1, 56, True)])
 def test_forward_host_head_groups_match_device_calls(sa, B, H, with_lse):
     # H >= 16 splits the layer into head groups whose copies overlap compute;
     # the result must be the one-call result bit for bit (the route and the

@@ -229,13 +229,18 @@ __global__ void __launch_bounds__(128) prologue_kernel(RouteArgs a, PrologueArgs
       }
       __syncthreads();
     }
-    for (int t = 0; t < nc; t += kT) {
-      uint4 xb[kT];
+    // the next kT tokens' loads are in flight while these are transformed
+    uint4 xb[kT], xn[kT];
+    auto load_batch = [&](int t, uint4* dst) {
 #pragma unroll
       for (int u = 0; u < kT; ++u)
-        xb[u] = (active && t + u < nc)
-                    ? *reinterpret_cast<const uint4*>(X + off + (t0 + c0 + t + u) * st[1])
-                    : make_uint4(0u, 0u, 0u, 0u);
+        dst[u] = (active && t + u < nc)
+                     ? *reinterpret_cast<const uint4*>(X + off + (t0 + c0 + t + u) * st[1])
+                     : make_uint4(0u, 0u, 0u, 0u);
+    };
+    load_batch(0, xb);
+    for (int t = 0; t < nc; t += kT) {
+      if (t + kT < nc) load_batch(t + kT, xn);
 #pragma unroll
       for (int u = 0; u < kT; ++u) {
         const uint32_t w[4] = {xb[u].x, xb[u].y, xb[u].z, xb[u].w};
@@ -278,6 +283,8 @@ __global__ void __launch_bounds__(128) prologue_kernel(RouteArgs a, PrologueArgs
           for (int v = 0; v < 8; ++v) two_sum(s[v], c[v], yr[v]);
         }
       }
+#pragma unroll
+      for (int u = 0; u < kT; ++u) xb[u] = xn[u];
     }
   }
   store_pooled<D>(a, which, b, h, d, i, nrow, n, s, c, active);

@@ -189,3 +189,13 @@ def test_prologue_and_pooled_route_reject_bad_arguments(sa):
     p.D = 96
     assert pro() == 2
     assert L.sa_route_pooled(ctypes.byref(p), a, a, 10, a, big, None, None) == 2
+
+
+def test_more_key_blocks_than_a_walk_holds_is_unsupported(sa):
+    L = sa.load_library()
+    p = params(sa, S=4096 * 64 + 1, H=1)          # 4097 key blocks
+    a = ctypes.c_void_p(4096)
+    assert L.sa_attn_dense(ctypes.byref(p), a, a, a, a, None, a, 1 << 40, None, None) == 2
+    assert L.sa_attn_sparse(ctypes.byref(p), a, a, a, a, a, a, None, a, 1 << 40, None, None) == 2
+    p = params(sa, S=4096 * 64, H=1)              # 4096: accepted up to the launch
+    assert L.sa_attn_workspace_bytes(ctypes.byref(p)) > 0

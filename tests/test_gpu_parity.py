@@ -364,3 +364,16 @@ def test_release_attention_is_deterministic_and_writes_every_row(sa, release):
     for o, lse in outs[1:]:
         assert torch.equal(o.view(torch.int16), o0.view(torch.int16))
         assert torch.equal(lse.view(torch.int32), l0.view(torch.int32))
+
+
+@pytest.mark.parametrize("S", [4096 * 64, 4096 * 64 - 17])
+def test_largest_supported_sequence(sa, S):
+    # 4096 key blocks is the most one attention tile's walk can list
+    # (kMaxNbAttn); the planner's shared-memory walk buffers are full here.
+    H, D, P, tau = 1, 128, 951, 1.2
+    q, k, v = sa_inputs.random_small(S, H, D, seed=5)
+    ref, rp, ci = check_route(sa, q, k, P, tau)
+    Nb = oracle.num_blocks(S)
+    assert Nb == 4096
+    cfg = sa_inputs.Config("max", S=S, P=P, H=H, D=D, tau=tau, kind="iid")
+    _sampled_attention_check(sa, cfg, q, k, v, ref["row_ptr"], ref["col_idx"], seed=6)

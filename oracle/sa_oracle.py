@@ -62,7 +62,7 @@ default):
   halves of a 128-token query block carry its key list, so step 7 is
   unchanged.
 
-The step before attention (SURVEY's fused prologue; "Making MiniMax-H3 up to
+The step before attention, fused with the pooling ("Making MiniMax-H3 up to
 9x faster on H100s", section "Custom kernels": a fused QK-norm plus RoPE
 kernel). The page names the two operations only; the reading used here:
 

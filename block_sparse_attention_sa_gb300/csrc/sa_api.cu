@@ -342,12 +342,13 @@ extern "C" {
 sa_status sa_route(const sa_params* p, const void* q, const void* k, int32_t* row_ptr,
                    int32_t* col_idx, int64_t col_cap, void* workspace, size_t ws_bytes,
                    int32_t* dev_status, void* stream) {
-  RouteArgs a;
-  const sa_status s = route_args(p, q, k, row_ptr, col_idx, col_cap, workspace, ws_bytes,
-                                 dev_status, &a);
+  sa_status s = check_params(p);
   if (s != SA_OK) return s;
   if (!q || !k || !row_ptr || !col_idx) return SA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k)) return SA_ERR_INVALID_ARG;
+  RouteArgs a;
+  s = route_args(p, q, k, row_ptr, col_idx, col_cap, workspace, ws_bytes, dev_status, &a);
+  if (s != SA_OK) return s;
   return from_cuda(launch_route(a, static_cast<cudaStream_t>(stream)));
 }
 
@@ -355,9 +356,7 @@ sa_status sa_qk_prologue(const sa_params* p, const void* q_in, const void* k_in,
                          const float* gamma_q, const float* gamma_k, float eps,
                          const float* rope_cos, const float* rope_sin, void* q_out, void* k_out,
                          void* workspace, size_t ws_bytes, int32_t* dev_status, void* stream) {
-  RouteArgs a;
-  const sa_status s = route_args(p, q_in, k_in, nullptr, nullptr, 0, workspace, ws_bytes,
-                                 dev_status, &a);
+  sa_status s = check_params(p);
   if (s != SA_OK) return s;
   if (!q_in || !k_in || !q_out || !k_out) return SA_ERR_INVALID_ARG;
   if (!aligned16(q_in) || !aligned16(k_in) || !aligned16(q_out) || !aligned16(k_out))
@@ -366,6 +365,9 @@ sa_status sa_qk_prologue(const sa_params* p, const void* q_in, const void* k_in,
   if ((rope_cos == nullptr) != (rope_sin == nullptr)) return SA_ERR_INVALID_ARG;
   if (rope_cos && (!aligned16(rope_cos) || !aligned16(rope_sin))) return SA_ERR_INVALID_ARG;
   if (!(eps >= 0.f) || !std::isfinite(eps)) return SA_ERR_INVALID_ARG;
+  RouteArgs a;
+  s = route_args(p, q_in, k_in, nullptr, nullptr, 0, workspace, ws_bytes, dev_status, &a);
+  if (s != SA_OK) return s;
   PrologueArgs pa{};
   pa.gamma_q = gamma_q;
   pa.gamma_k = gamma_k;
@@ -380,11 +382,13 @@ sa_status sa_qk_prologue(const sa_params* p, const void* q_in, const void* k_in,
 sa_status sa_route_pooled(const sa_params* p, int32_t* row_ptr, int32_t* col_idx,
                           int64_t col_cap, void* workspace, size_t ws_bytes, int32_t* dev_status,
                           void* stream) {
-  RouteArgs a;
-  const sa_status s = route_args(p, nullptr, nullptr, row_ptr, col_idx, col_cap, workspace,
-                                 ws_bytes, dev_status, &a);
+  sa_status s = check_params(p);
   if (s != SA_OK) return s;
   if (!row_ptr || !col_idx) return SA_ERR_INVALID_ARG;
+  RouteArgs a;
+  s = route_args(p, nullptr, nullptr, row_ptr, col_idx, col_cap, workspace, ws_bytes, dev_status,
+                 &a);
+  if (s != SA_OK) return s;
   return from_cuda(launch_route_select(a, static_cast<cudaStream_t>(stream)));
 }
 

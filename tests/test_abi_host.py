@@ -112,6 +112,9 @@ def test_null_and_misaligned_pointers_rejected(sa):
     p = params(sa)
     a = ctypes.c_void_p(4096)
     assert L.sa_route(ctypes.byref(p), None, a, a, a, 10, a, 1 << 40, None, None) == 1
+    # a missing pointer is reported before a short workspace
+    assert L.sa_route(ctypes.byref(p), None, a, a, a, 10, a, 16, None, None) == 1
+    assert L.sa_route(ctypes.byref(p), a, a, a, a, 10, a, 16, None, None) == 3
     assert L.sa_route(ctypes.byref(p), ctypes.c_void_p(4098), a, a, a, 10, a, 1 << 40,
                       None, None) == 1
     assert L.sa_route(ctypes.byref(p), a, a, a, a, 10, ctypes.c_void_p(4096 + 16), 1 << 40,

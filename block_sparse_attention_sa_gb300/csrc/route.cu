@@ -762,7 +762,9 @@ cudaError_t launch_select_d(const RouteArgs& a, cudaStream_t st) {
                                static_cast<int>(smem));
       if (e != cudaSuccess) return e;
     }
-    recheck_kernel<D><<<sms, kRecheckThreads, smem, st>>>(a);
+    // two queued rows per SM at a time: a top-mass row spends part of its
+    // time in one warp's bisection, which the other row's warps overlap
+    recheck_kernel<D><<<2 * sms, kRecheckThreads, smem, st>>>(a);
   }
   scan_kernel<<<1, 1024, 0, st>>>(a);
   emit_kernel<<<static_cast<unsigned>((L.rows + 7) / 8), 256, 0, st>>>(a);

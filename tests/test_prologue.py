@@ -162,3 +162,34 @@ def test_release_prologue_route_and_sampled_outputs(sa, qb):
     heads = [0, 31, 55]
     sub = lambda t: t[:, :, heads].contiguous()
     check_outputs(sub(q), sub(k), sub(qo.cpu()), sub(ko.cpu()), gq, gk, 1e-6, cos, sin)
+
+
+def test_batch_and_strided_views(sa):
+    # B = 2, heads 1..3 of a 5-head buffer: non-contiguous b/s/h strides, out of place
+    # into tensors of the same strides, and in place
+    S, D = 300, 128
+    g = torch.Generator().manual_seed(21)
+    big = [torch.randn((2, S, 5, D), generator=g).to(torch.bfloat16) for _ in range(2)]
+    q, k = (t[:, :, 1:4, :] for t in big)
+    gq, gk = sa_inputs.qk_norm_weights(D, seed=4)
+    cfg = sa_inputs.Config("t", S=S, P=0, H=3, D=D, tau=1.0, kind="iid")
+    cos, sin = sa_inputs.rope_tables(cfg)
+    bigd = [t.cuda() for t in big]
+    qd, kd = (t[:, :, 1:4, :] for t in bigd)
+    assert not qd.is_contiguous()
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    qo, ko, ws = sa.sa_qk_prologue(qd, kd, gq.cuda(), gk.cuda(), 1e-6, cos.cuda(), sin.cuda(),
+                                   dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0 and qo.stride() == qd.stride()
+    check_outputs(q, k, qo, ko, gq, gk, 1e-6, cos, sin)
+    check_routes(sa, qo, ko, ws, 64, 1.0, 64)
+    sa.sa_qk_prologue(qd, kd, gq.cuda(), gk.cuda(), 1e-6, cos.cuda(), sin.cuda(), q_out=qd,
+                      k_out=kd, dev_status=st)
+    torch.cuda.synchronize()
+    assert torch.equal(qd.view(torch.int16), qo.view(torch.int16))
+    assert torch.equal(kd.view(torch.int16), ko.view(torch.int16))
+    # the other heads of the buffers are untouched
+    for t, td in zip(big, bigd):
+        for h in (0, 4):
+            assert torch.equal(td[:, :, h].cpu().view(torch.int16), t[:, :, h].view(torch.int16))

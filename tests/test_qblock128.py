@@ -132,3 +132,24 @@ def test_release_route_bitexact_and_attention_sampled(sa):
     l2, mx, _ = out_errors(og, orf)
     assert l2 <= L2_TOL and mx <= MAXABS_TOL, (l2, mx)
     assert lse_ok(lg, lrf)
+
+
+def test_batch_and_strided_views(sa):
+    # B = 2, heads 1..3 of a 5-head buffer, a ragged S: non-contiguous b/s/h strides
+    g = torch.Generator().manual_seed(12)
+    big = [torch.randn((2, 333, 5, 64), generator=g).to(torch.bfloat16) for _ in range(3)]
+    q, k, v = (t[:, :, 1:4, :] for t in big)
+    qd, kd, vd = (t.cuda()[:, :, 1:4, :] for t in big)
+    assert not qd.is_contiguous()
+    ref = oracle.route_ref(q, k, 70, f32(0.9), q_block=128)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rp, ci = sa.sa_route(qd, kd, 70, 0.9, q_block=128, dev_status=st)
+    o, lse = sa.sa_attn_sparse(qd, kd, vd, rp, ci, q_block=128, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    rpn, cin = to_np(rp).astype(np.int64), to_np(ci).astype(np.int64)
+    bad, _ = compare_route(rpn, cin[:rpn[-1]], ref, 2, 3, oracle.num_blocks(333))
+    assert bad == 0
+    o_ref, lse_ref = oracle.attn_ref(q, k, v, rpn, cin)
+    l2, mx, _ = out_errors(to_np(o), o_ref)
+    assert l2 <= L2_TOL and mx <= MAXABS_TOL and lse_ok(to_np(lse), lse_ref)

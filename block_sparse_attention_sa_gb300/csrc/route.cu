@@ -762,9 +762,11 @@ cudaError_t launch_select_d(const RouteArgs& a, cudaStream_t st) {
                                static_cast<int>(smem));
       if (e != cudaSuccess) return e;
     }
-    // two queued rows per SM at a time: a top-mass row spends part of its
-    // time in one warp's bisection, which the other row's warps overlap
-    recheck_kernel<D><<<2 * sms, kRecheckThreads, smem, st>>>(a);
+    // top-mass: two queued rows per SM at a time (a row spends part of its
+    // time in one warp's bisection, which the other row's warps overlap);
+    // otherwise one, so that a row's dot products have the fp64 unit alone
+    const int per_sm = a.mode == SA_ROUTE_TOP_MASS ? 2 : 1;
+    recheck_kernel<D><<<per_sm * sms, kRecheckThreads, smem, st>>>(a);
   }
   scan_kernel<<<1, 1024, 0, st>>>(a);
   emit_kernel<<<static_cast<unsigned>((L.rows + 7) / 8), 256, 0, st>>>(a);

@@ -153,3 +153,24 @@ def test_batch_and_strided_views(sa):
     o_ref, lse_ref = oracle.attn_ref(q, k, v, rpn, cin)
     l2, mx, _ = out_errors(to_np(o), o_ref)
     assert l2 <= L2_TOL and mx <= MAXABS_TOL and lse_ok(to_np(lse), lse_ref)
+
+
+def test_forward_host_matches_device_calls(sa):
+    # the whole layer from pinned host memory, in head groups, with 128-token
+    # query blocks: bit for bit the result of the two device calls
+    B, S, H, D, P, tau = 1, 1000, 24, 128, 100, 1.0
+    q, k, v = sa_inputs.random_small(S, H, D, seed=77)
+    bufs = sa.alloc_layer_buffers(B, S, H, D)
+    qh, kh, vh = (t.contiguous().pin_memory() for t in (q, k, v))
+    lse_host = torch.empty((B, H, S), dtype=torch.float32).pin_memory()
+    o_host = sa.sa_forward_host(qh, kh, vh, P, tau, bufs=bufs, q_block=128, lse_host=lse_host)
+    torch.cuda.synchronize()
+    assert int(bufs["status"].item()) == 0
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    rp, ci = sa.sa_route(qd, kd, P, tau, q_block=128, dev_status=st)
+    o, lse = sa.sa_attn_sparse(qd, kd, vd, rp, ci, q_block=128, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert torch.equal(o_host.view(torch.int16), o.cpu().view(torch.int16))
+    assert torch.equal(lse_host.view(torch.int32), lse.cpu().view(torch.int32))

@@ -50,7 +50,7 @@ EXPORTS = (
     "sa_params_init", "sa_num_blocks", "sa_route_rows", "sa_route_max_nnz",
     "sa_route_workspace_bytes", "sa_route", "sa_attn_workspace_bytes", "sa_attn_sparse",
     "sa_attn_dense", "sa_forward_host", "sa_dev_status_decode", "sa_status_string",
-    "sa_route_static", "sa_qk_prologue", "sa_route_pooled",
+    "sa_route_static", "sa_qk_prologue", "sa_route_pooled", "sa_check_wait_timeout",
 )
 SA_ROUTE_STATIC_WS_BYTES = 32 << 20
 
@@ -106,6 +106,7 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         "sa_forward_host": (ctypes.c_int, [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i64,
                                            vp, sz, vp, vp]),
         "sa_dev_status_decode": (ctypes.c_int, [ctypes.c_int32]),
+        "sa_check_wait_timeout": (ctypes.c_int, [vp, vp]),
         "sa_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     }
     for name, (res, args) in sig.items():

@@ -313,6 +313,16 @@ sa_status sa_forward_host(const sa_params* p, const void* q_host,
                           void* workspace, size_t ws_bytes,
                           int32_t* dev_status, void* stream);
 
+/*
+ * sa_check_wait_timeout -- a device check of the failure path that every
+ * pipeline wait of this library shares (no counterpart on the pages): it
+ * launches one warp that waits on a barrier nothing completes. The wait gives
+ * up after the library's time limit (250 ms), OR-s SA_DEV_TIMEOUT into
+ * *dev_status (device memory, required) and the kernel returns; the context
+ * stays usable. Nothing faults, traps or hangs. Asynchronous on `stream`.
+ */
+sa_status sa_check_wait_timeout(int32_t* dev_status, void* stream);
+
 /* Decodes *dev_status bits into the most severe sa_status (SA_OK if 0). */
 sa_status sa_dev_status_decode(int32_t dev_status);
 

@@ -202,3 +202,8 @@ def test_more_key_blocks_than_a_walk_holds_is_unsupported(sa):
     assert L.sa_attn_sparse(ctypes.byref(p), a, a, a, a, a, a, None, a, 1 << 40, None, None) == 2
     p = params(sa, S=4096 * 64, H=1)              # 4096: accepted up to the launch
     assert L.sa_attn_workspace_bytes(ctypes.byref(p)) > 0
+
+
+def test_wait_check_needs_a_status_word(sa):
+    L = sa.load_library()
+    assert L.sa_check_wait_timeout(None, None) == 1

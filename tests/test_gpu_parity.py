@@ -377,3 +377,17 @@ def test_largest_supported_sequence(sa, S):
     assert Nb == 4096
     cfg = sa_inputs.Config("max", S=S, P=P, H=H, D=D, tau=tau, kind="iid")
     _sampled_attention_check(sa, cfg, q, k, v, ref["row_ptr"], ref["col_idx"], seed=6)
+
+
+def test_bounded_wait_reports_timeout_and_the_context_survives(sa):
+    # one warp waits on a barrier nothing completes: the wait gives up after
+    # its limit and reports SA_DEV_TIMEOUT, and later work runs normally
+    L = sa.load_library()
+    st = new_status()
+    assert L.sa_check_wait_timeout(st.data_ptr(), torch.cuda.current_stream().cuda_stream) == 0
+    torch.cuda.synchronize()
+    assert int(st.item()) & sa.SA_DEV_TIMEOUT
+    assert L.sa_dev_status_decode(int(st.item())) == 5          # SA_ERR_TIMEOUT
+    cfg, q, k, v = sa_inputs.make_inputs("tiny")
+    ref, rp, ci = check_route(sa, q, k, cfg.P, cfg.tau)
+    check_attn_full(sa, q, k, v, rp, ci[:rp[-1]])

@@ -27,7 +27,7 @@ import torch
 
 __all__ = [
     "SaError", "load_library", "library_path", "sa_params", "make_params", "sa_route",
-    "sa_qk_prologue", "sa_route_pooled",
+    "sa_qk_prologue", "sa_route_pooled", "sa_attn_prepare", "sa_attn_run",
     "sa_attn_sparse", "sa_attn_dense", "sa_forward_host", "sa_route_workspace_bytes",
     "sa_attn_workspace_bytes", "sa_route_max_nnz", "check_dev_status", "EXPORTS",
     "SA_DEV_CAPACITY", "SA_DEV_TIMEOUT", "SA_DEV_BAD_ROUTE", "SA_DEV_RANGE",
@@ -51,6 +51,7 @@ EXPORTS = (
     "sa_route_workspace_bytes", "sa_route", "sa_attn_workspace_bytes", "sa_attn_sparse",
     "sa_attn_dense", "sa_forward_host", "sa_dev_status_decode", "sa_status_string",
     "sa_route_static", "sa_qk_prologue", "sa_route_pooled", "sa_check_wait_timeout",
+    "sa_attn_prepare", "sa_attn_run",
 )
 SA_ROUTE_STATIC_WS_BYTES = 32 << 20
 
@@ -107,6 +108,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
                                            vp, sz, vp, vp]),
         "sa_dev_status_decode": (ctypes.c_int, [ctypes.c_int32]),
         "sa_check_wait_timeout": (ctypes.c_int, [vp, vp]),
+        "sa_attn_prepare": (ctypes.c_int, [P, vp, vp, vp, vp, sz, vp, vp]),
+        "sa_attn_run": (ctypes.c_int, [P, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp]),
         "sa_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     }
     for name, (res, args) in sig.items():
@@ -299,6 +302,41 @@ def sa_attn_sparse(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, row_ptr: t
                               _ptr(col_idx), _ptr(o), _ptr(lse), _ptr(ws),
                               ws.numel() * ws.element_size(), _ptr(dev_status), _stream(stream))
     _check(code, "sa_attn_sparse")
+    return o, lse
+
+
+def sa_attn_prepare(v: torch.Tensor, row_ptr: torch.Tensor, col_idx: torch.Tensor, *,
+                    workspace: torch.Tensor, q_block: int = 64,
+                    dev_status: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """First half of sa_attn_sparse: V repacked into ``workspace`` and the
+    tile pairs chosen from the route. Returns the workspace."""
+    _require_cuda(v, row_ptr, col_idx, workspace)
+    p = make_params(v, v, v, v, q_block=q_block)
+    if workspace.numel() * workspace.element_size() < sa_attn_workspace_bytes(p):
+        raise ValueError("workspace too small")
+    code = load_library().sa_attn_prepare(ctypes.byref(p), _ptr(v), _ptr(row_ptr), _ptr(col_idx),
+                                          _ptr(workspace),
+                                          workspace.numel() * workspace.element_size(),
+                                          _ptr(dev_status), _stream(stream))
+    _check(code, "sa_attn_prepare")
+    return workspace
+
+
+def sa_attn_run(q: torch.Tensor, k: torch.Tensor, row_ptr: torch.Tensor, col_idx: torch.Tensor,
+                scale: float = 0.0, *, workspace: torch.Tensor, v_like: Optional[torch.Tensor] = None,
+                o: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                want_lse: bool = True, q_block: int = 64,
+                dev_status: Optional[torch.Tensor] = None, stream=None):
+    """Second half of sa_attn_sparse: the attention kernel over a workspace
+    sa_attn_prepare filled. ``v_like`` gives V's strides (default q's)."""
+    _require_cuda(q, k, row_ptr, col_idx, workspace)
+    o, lse = _attn_out(q, o, lse, want_lse)
+    p = make_params(q, k, v_like, o, scale=scale, q_block=q_block)
+    code = load_library().sa_attn_run(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(row_ptr),
+                                      _ptr(col_idx), _ptr(o), _ptr(lse), _ptr(workspace),
+                                      workspace.numel() * workspace.element_size(),
+                                      _ptr(dev_status), _stream(stream))
+    _check(code, "sa_attn_run")
     return o, lse
 
 

@@ -126,43 +126,45 @@ AttnLayout attn_layout(const sa_params* p) {
 
 size_t attn_ws_bytes(const sa_params* p) { return attn_layout(p).total; }
 
-sa_status attn_common(const sa_params* p, const void* q, const void* k, const void* v,
-                      const int32_t* row_ptr, const int32_t* col_idx, void* o, float* lse,
-                      void* ws, size_t ws_bytes, int32_t* dev_status, void* stream, bool dense) {
-  sa_status s = check_params(p);
+// The launch-time checks of the attention calls (q, k, o unchecked when
+// null_qko_ok: sa_attn_prepare does not take them).
+sa_status attn_check(const sa_params* p, const void* q, const void* k, const void* v,
+                     const int32_t* row_ptr, const int32_t* col_idx, const void* o,
+                     const void* ws, size_t ws_bytes, bool dense, bool need_v, bool need_qko) {
+  const sa_status s = check_params(p);
   if (s != SA_OK) return s;
-  if (!q || !k || !v || !o || !ws) return SA_ERR_INVALID_ARG;
+  if (!ws || (need_v && !v) || (need_qko && (!q || !k || !o))) return SA_ERR_INVALID_ARG;
   if (!dense && (!row_ptr || !col_idx)) return SA_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return SA_ERR_INVALID_ARG;
+  if ((need_v && !aligned16(v)) || (need_qko && (!aligned16(q) || !aligned16(k) || !aligned16(o))))
+    return SA_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return SA_ERR_INVALID_ARG;
   if (!strides_ok(p->q_stride) || !strides_ok(p->k_stride) || !strides_ok(p->v_stride) ||
       !strides_ok(p->o_stride))
     return SA_ERR_INVALID_ARG;
-  const int Nb = num_blocks(p->S);
-  if (Nb > kMaxNbAttn) return SA_ERR_UNSUPPORTED;
+  if (num_blocks(p->S) > kMaxNbAttn) return SA_ERR_UNSUPPORTED;
   if (ws_bytes < attn_ws_bytes(p)) return SA_ERR_CAPACITY;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  return SA_OK;
+}
 
-  AttnMaps maps;
-  std::memset(&maps, 0, sizeof(maps));
-  if ((s = encode_bshd(&maps.q, q, p, p->q_stride)) != SA_OK) return s;
-  if ((s = encode_bshd(&maps.k, k, p, p->k_stride)) != SA_OK) return s;
-  if ((s = encode_vt(&maps.vt, ws, p)) != SA_OK) return s;
+// Tiles of two 64-token query blocks are paired from the route; a route of
+// 128-token query blocks gives both halves of each tile (2i, 2i + 1) the
+// same list, so the neighbour tiles are then exact.
+bool uses_pairing(const sa_params* p, bool dense) {
+  return !dense && num_blocks(p->S) > 2 && q_block_of(*p) == kBlock;
+}
 
-  cudaError_t e = launch_pack_v(static_cast<const uint16_t*>(v), p->v_stride, p->B, p->S, p->H,
-                                p->D, s_pad_of(p->S), static_cast<uint16_t*>(ws), dev_status, st);
-  if (e != cudaSuccess) return SA_ERR_CUDA;
-
-  const AttnLayout L = attn_layout(p);
-  char* wsb = static_cast<char*>(ws);
-  AttnArgs a{};
-  a.row_ptr = dense ? nullptr : row_ptr;
-  a.col_idx = dense ? nullptr : col_idx;
-  a.pairs = nullptr;
-  if (!dense && Nb > 2 && q_block_of(*p) == kBlock) {
-    // choose the query-block pairs of the 128-row tiles from the route (a
-    // route of 128-token query blocks gives both halves of each tile
-    // (2i, 2i + 1) the same list: the neighbour tiles are then exact)
+// First half of an attention call: V repacked into the workspace, and the
+// tile pairs chosen from the route.
+sa_status attn_prepare_launch(const sa_params* p, const void* v, const int32_t* row_ptr,
+                              const int32_t* col_idx, void* ws, int32_t* dev_status,
+                              cudaStream_t st, bool dense) {
+  if (launch_pack_v(static_cast<const uint16_t*>(v), p->v_stride, p->B, p->S, p->H, p->D,
+                    s_pad_of(p->S), static_cast<uint16_t*>(ws), dev_status, st) != cudaSuccess)
+    return SA_ERR_CUDA;
+  if (uses_pairing(p, dense)) {
+    const AttnLayout L = attn_layout(p);
+    char* wsb = static_cast<char*>(ws);
+    const int Nb = num_blocks(p->S);
     PairArgs pa{};
     pa.row_ptr = row_ptr;
     pa.col_idx = col_idx;
@@ -171,8 +173,27 @@ sa_status attn_common(const sa_params* p, const void* q, const void* k, const vo
     pa.Nb = Nb;
     pa.n_pairs = (Nb + 1) / 2;
     if (launch_pair(pa, p->B * p->H, st) != cudaSuccess) return SA_ERR_CUDA;
-    a.pairs = pa.pairs;
   }
+  return SA_OK;
+}
+
+// Second half: the attention kernel over the prepared workspace.
+sa_status attn_run_launch(const sa_params* p, const void* q, const void* k,
+                          const int32_t* row_ptr, const int32_t* col_idx, void* o, float* lse,
+                          void* ws, int32_t* dev_status, cudaStream_t st, bool dense) {
+  sa_status s;
+  AttnMaps maps;
+  std::memset(&maps, 0, sizeof(maps));
+  if ((s = encode_bshd(&maps.q, q, p, p->q_stride)) != SA_OK) return s;
+  if ((s = encode_bshd(&maps.k, k, p, p->k_stride)) != SA_OK) return s;
+  if ((s = encode_vt(&maps.vt, ws, p)) != SA_OK) return s;
+  const AttnLayout L = attn_layout(p);
+  char* wsb = static_cast<char*>(ws);
+  const int Nb = num_blocks(p->S);
+  AttnArgs a{};
+  a.row_ptr = dense ? nullptr : row_ptr;
+  a.col_idx = dense ? nullptr : col_idx;
+  a.pairs = uses_pairing(p, dense) ? reinterpret_cast<uint32_t*>(wsb + L.pairs) : nullptr;
   a.o = static_cast<uint16_t*>(o);
   a.lse = lse;
   a.dev_status = dev_status;
@@ -187,6 +208,17 @@ sa_status attn_common(const sa_params* p, const void* q, const void* k, const vo
   a.tile_counter = reinterpret_cast<int*>(wsb + L.counter);
   if (cudaMemsetAsync(a.tile_counter, 0, sizeof(int), st) != cudaSuccess) return SA_ERR_CUDA;
   return from_cuda(launch_attn(p->D, maps, a, st));
+}
+
+sa_status attn_common(const sa_params* p, const void* q, const void* k, const void* v,
+                      const int32_t* row_ptr, const int32_t* col_idx, void* o, float* lse,
+                      void* ws, size_t ws_bytes, int32_t* dev_status, void* stream, bool dense) {
+  sa_status s = attn_check(p, q, k, v, row_ptr, col_idx, o, ws, ws_bytes, dense, true, true);
+  if (s != SA_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if ((s = attn_prepare_launch(p, v, row_ptr, col_idx, ws, dev_status, st, dense)) != SA_OK)
+    return s;
+  return attn_run_launch(p, q, k, row_ptr, col_idx, o, lse, ws, dev_status, st, dense);
 }
 
 // sa_forward_host's copy streams and events, created on first use on each
@@ -397,6 +429,26 @@ sa_status sa_attn_sparse(const sa_params* p, const void* q, const void* k, const
                          void* workspace, size_t ws_bytes, int32_t* dev_status, void* stream) {
   return attn_common(p, q, k, v, row_ptr, col_idx, o, lse, workspace, ws_bytes, dev_status, stream,
                      false);
+}
+
+sa_status sa_attn_prepare(const sa_params* p, const void* v, const int32_t* row_ptr,
+                          const int32_t* col_idx, void* workspace, size_t ws_bytes,
+                          int32_t* dev_status, void* stream) {
+  const sa_status s = attn_check(p, nullptr, nullptr, v, row_ptr, col_idx, nullptr, workspace,
+                                 ws_bytes, false, true, false);
+  if (s != SA_OK) return s;
+  return attn_prepare_launch(p, v, row_ptr, col_idx, workspace, dev_status,
+                             static_cast<cudaStream_t>(stream), false);
+}
+
+sa_status sa_attn_run(const sa_params* p, const void* q, const void* k, const int32_t* row_ptr,
+                      const int32_t* col_idx, void* o, float* lse, void* workspace,
+                      size_t ws_bytes, int32_t* dev_status, void* stream) {
+  const sa_status s = attn_check(p, q, k, nullptr, row_ptr, col_idx, o, workspace, ws_bytes,
+                                 false, false, true);
+  if (s != SA_OK) return s;
+  return attn_run_launch(p, q, k, row_ptr, col_idx, o, lse, workspace, dev_status,
+                         static_cast<cudaStream_t>(stream), false);
 }
 
 sa_status sa_attn_dense(const sa_params* p, const void* q, const void* k, const void* v, void* o,

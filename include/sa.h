@@ -276,6 +276,23 @@ sa_status sa_attn_sparse(const sa_params* p, const void* q, const void* k,
                          void* stream);
 
 /*
+ * sa_attn_prepare, sa_attn_run -- sa_attn_sparse in two calls, with the same
+ * result: sa_attn_prepare repacks V into the workspace and (for 64-token
+ * query blocks) chooses the tile pairs from the route; sa_attn_run launches
+ * the attention kernel over that workspace. Between them the caller may
+ * enqueue other work (or time the kernel alone); sa_attn_run must see the
+ * same p, route and workspace, after sa_attn_prepare on the same stream (or
+ * ordered after it), and V unchanged. Arguments and errors as
+ * sa_attn_sparse, each call checking what it takes.
+ */
+sa_status sa_attn_prepare(const sa_params* p, const void* v, const int32_t* row_ptr,
+                          const int32_t* col_idx, void* workspace, size_t ws_bytes,
+                          int32_t* dev_status, void* stream);
+sa_status sa_attn_run(const sa_params* p, const void* q, const void* k,
+                      const int32_t* row_ptr, const int32_t* col_idx, void* o, float* lse,
+                      void* workspace, size_t ws_bytes, int32_t* dev_status, void* stream);
+
+/*
  * sa_attn_dense -- the same forward with every key block attended (density
  * 100%), as the pages run for the first denoising steps and the first layers
  * (Sol-Engine H3-DataCenter release page, policy paragraph). Arguments as in

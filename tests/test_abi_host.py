@@ -207,3 +207,16 @@ def test_more_key_blocks_than_a_walk_holds_is_unsupported(sa):
 def test_wait_check_needs_a_status_word(sa):
     L = sa.load_library()
     assert L.sa_check_wait_timeout(None, None) == 1
+
+
+def test_prepare_and_run_check_their_own_arguments(sa):
+    L = sa.load_library()
+    p = params(sa)
+    a = ctypes.c_void_p(4096)
+    big = 1 << 40
+    assert L.sa_attn_prepare(ctypes.byref(p), None, a, a, a, big, None, None) == 1   # no V
+    assert L.sa_attn_prepare(ctypes.byref(p), a, None, a, a, big, None, None) == 1   # no route
+    assert L.sa_attn_prepare(ctypes.byref(p), a, a, a, a, 1024, None, None) == 3     # short ws
+    assert L.sa_attn_run(ctypes.byref(p), None, a, a, a, a, None, a, big, None, None) == 1
+    assert L.sa_attn_run(ctypes.byref(p), a, a, a, a, None, None, a, big, None, None) == 1
+    assert L.sa_attn_run(ctypes.byref(p), a, a, a, a, a, None, a, 1024, None, None) == 3

@@ -391,3 +391,24 @@ def test_bounded_wait_reports_timeout_and_the_context_survives(sa):
     cfg, q, k, v = sa_inputs.make_inputs("tiny")
     ref, rp, ci = check_route(sa, q, k, cfg.P, cfg.tau)
     check_attn_full(sa, q, k, v, rp, ci[:rp[-1]])
+
+
+@pytest.mark.parametrize("name,q_block", [("tiny", 64), ("mid", 64), ("mid", 128)])
+def test_prepare_then_run_equals_attn_sparse(sa, name, q_block):
+    # sa_attn_sparse in its two halves, other work enqueued in between: the
+    # same output bit for bit
+    cfg, q, k, v = sa_inputs.make_inputs(name)
+    qd, kd, vd = dev(q, k, v)
+    st = new_status()
+    rp, ci = sa.sa_route(qd, kd, cfg.P, cfg.tau, q_block=q_block, dev_status=st)
+    o, lse = sa.sa_attn_sparse(qd, kd, vd, rp, ci, q_block=q_block, dev_status=st)
+    p = sa.make_params(qd, kd, vd, o, q_block=q_block)
+    ws = torch.empty(sa.sa_attn_workspace_bytes(p), dtype=torch.uint8, device="cuda")
+    sa.sa_attn_prepare(vd, rp, ci, workspace=ws, q_block=q_block, dev_status=st)
+    junk = torch.randn(1 << 20, device="cuda").sum()        # unrelated work in between
+    o2, lse2 = sa.sa_attn_run(qd, kd, rp, ci, workspace=ws, v_like=vd, q_block=q_block,
+                              dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0 and torch.isfinite(junk)
+    assert torch.equal(o.view(torch.int16), o2.view(torch.int16))
+    assert torch.equal(lse.view(torch.int32), lse2.view(torch.int32))

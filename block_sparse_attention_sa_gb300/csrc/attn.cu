@@ -7,7 +7,7 @@
 // execution", third paragraph: the exact prefix sink and the diagonal are
 // part of every route). Dense mode lists every key block.
 //
-// Tiles. A tile is a 128-row query tile = query blocks 2p and 2p+1 of one
+// Tiles. A tile is a 128-row query tile = two 64-token query blocks of one
 // head (tcgen05 M = 128; the route is per 64-row block). Its key walk is the
 // union of the two blocks' key lists, two 64-key blocks per step (N = 128);
 // a key block listed for only one of the two query blocks is masked to -inf
@@ -25,25 +25,29 @@
 // the softmax turns it into P (fp16) over the same columns; O += P V(j)
 // (fp16, A from TMEM). The MMA warp issues QK^T(j+2) before it waits for
 // P(j) -- its buffer last held step j-1, whose PV was issued already -- so
-// the tensor pipe has the next products queued while the softmax works and
-// the softmax always finds its next S ready: the step rate is set by the
-// slower of the tensor pipe and the softmax, not by their sum.
+// the tensor pipe has the next products queued while the softmax works.
 //
-// Softmax. Eight warps; the two threads of a row (warps q and q+4 share
-// TMEM lane quarter q) take one 64-key block of the step each. They agree on
-// the row's running max through shared memory and a named barrier for the
-// pair, keep their own partial row sums, and each rescales and writes its
-// half of O's columns. The running max moves only when a block max exceeds
-// it by more than 2^14 (then O is rescaled, after the last PV into it has
-// completed).
+// Softmax. Two warpgroups take the steps in turn (warpgroup 0 the even
+// steps of this CTA's sequence, warpgroup 1 the odd ones), one thread per
+// row with all 128 keys of its step, so each warpgroup has two steps' time
+// for one step's chain. The rows' running max passes from step to step
+// through shared memory: a thread publishes the max after its step as soon
+// as it knows it, and the thread of the next step reads it before its
+// exponentials (it seldom waits: the previous step started a whole step
+// earlier). Each warpgroup keeps its own partial row sum; the two threads of
+// a row add them in the epilogue. The running max moves only when a block
+// max exceeds it by more than 2^14 (then O is rescaled, after the last PV
+// into it has completed).
 //
-// Warps: 0-7 softmax, 8 producer (Q, and K and V through one ring of
-// stages in the order the MMA warp consumes them), 9 MMA (converged;
-// elect.sync issues), 10 planner, 11 idle. No data-dependent load sits inside
-// a pipelined loop: the walk is built ahead by the planner. Every mbarrier
-// wait is bounded (SA_DEV_TIMEOUT); the softmax pairs carry a stop bit
-// through each exchange so both warps of a pair leave together, and an
-// aborted CTA drains its own copies and MMAs and frees TMEM before it exits.
+// Warps: 0-3 softmax of even steps, 4-7 of odd steps, 8 producer (Q, and K and
+// V through one ring of stages in the order the MMA warp consumes them),
+// 9 MMA (converged; elect.sync issues), 10 planner, 11 idle. No
+// data-dependent load sits inside a pipelined loop: the walk is built ahead
+// by the planner. Every wait is bounded (SA_DEV_TIMEOUT); the two threads of
+// a row carry a stop bit through both of their exchanges so they always
+// leave together, and an aborted CTA drains its own copies and MMAs and
+// frees TMEM before it exits.
+#include <climits>
 #include <cmath>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -59,17 +63,20 @@ constexpr int BM = 128;   // query rows per tile
 constexpr int BN = 128;   // key rows per step (two key blocks)
 constexpr int KVST = 5;   // stages of the K/V ring (each holds one K or one V^T tile of a step)
 constexpr int kSBuf = 3;  // S buffers in TMEM
-constexpr int kThreads = 384;   // three warpgroups: softmax (two), control
-constexpr int kSoftmaxThreads = 256;
+constexpr int kSets = 2;  // softmax warpgroups, taking the steps in turn
+constexpr int kThreads = 384;        // three warpgroups: softmax (two), control
+constexpr int kSetThreads = 128;     // one softmax thread per row and warpgroup
+constexpr int kSoftmaxThreads = kSets * kSetThreads;
 constexpr int kProducerWarp = 8, kMmaWarp = 9, kPlannerWarp = 10;  // warp 11: barriers only
 // Register split (setmaxnreg). At launch ptxas gives every thread
 // kLaunchRegs (65536 / 384 rounded down to a multiple of 8); the two softmax
 // warpgroups then grow to kSoftmaxRegs and the control warpgroup shrinks
-// to kControlRegs: 2*128*208 + 128*80 = 63,488 <= 384*168 = 64,512, and per
-// SM sub-partition (one warp of each warpgroup) 208 + 208 + 80 <= 512.
+// to kControlRegs: 2*128*216 + 128*64 = 63,488 <= 384*168 = 64,512, and per
+// SM sub-partition (one warp of each warpgroup) 216 + 216 + 64 <= 512. A
+// softmax thread holds a whole 128-key row of S (128 registers) at once.
 constexpr int kLaunchRegs = 168;
-constexpr int kSoftmaxRegs = 208;
-constexpr int kControlRegs = 80;
+constexpr int kSoftmaxRegs = 216;
+constexpr int kControlRegs = 64;
 static_assert(2 * 128 * kSoftmaxRegs + 128 * kControlRegs <= kThreads * kLaunchRegs,
               "register split exceeds the launch allocation");
 constexpr int kTmemCols = 512;
@@ -106,8 +113,14 @@ struct Smem {
   static constexpr int kNumBars = bFin + 1;
   static constexpr int kMisc = kBar + kNumBars * 8;   // tmem base, abort flag
   static constexpr int kHdr = kMisc + 16;             // [2][4] walk headers: b, h, pair, n
-  static constexpr int kXch = kHdr + 32;              // pair exchange: [2 slots][2 halves][BM] x 2 words
-  static constexpr int kBits = kXch + 2 * 2 * BM * 8;
+  // row exchange: [2 slots][2 warpgroups][BM] of (m, l, stop)
+  static constexpr int kXch = kHdr + 32;
+  static constexpr int kXchBytes = 2 * kSets * BM * 12;
+  // running-max handoff: [2 warpgroups][BM] max after the warpgroup's latest
+  // step, and that step's index in the CTA's sequence
+  static constexpr int kHand = kXch + kXchBytes;
+  static constexpr int kHandBytes = kSets * BM * 8;
+  static constexpr int kBits = kHand + kHandBytes;
   static constexpr int kInfo = kBits + 2 * (kMaxNbAttn / 32) * 4;  // [2][kMaxNbAttn] walks
   static constexpr int kEnd = kInfo + 2 * kMaxNbAttn * 2;
   static constexpr int kBytes = kEnd + 1024;          // slack to align the base to 1 KB
@@ -131,7 +144,7 @@ __device__ __forceinline__ void set_status(int32_t* st, int bits) {
 // gives up, so a status word names the stage that stalled.
 enum WaitSite {
   kSiteKVStage = 0, kSiteQFull, kSiteKVFull, kSitePFull, kSiteSFull, kSiteFin, kSiteInfo,
-  kSiteOFree, kSitePVDone
+  kSiteOFree, kSitePVDone, kSiteHandoff
 };
 
 __device__ __forceinline__ bool elect_one() {
@@ -145,30 +158,29 @@ __device__ __forceinline__ void note_timeout(int32_t* st, int site) {
   set_status(st, SA_DEV_TIMEOUT | (1 << (8 + site)));
 }
 
-// max over 64 fp32 values (bit patterns): eight chains of three-input max.
-__device__ __forceinline__ float max64(const uint32_t* v) {
-  float m[8];
+// max over 32 fp32 values (bit patterns): four chains of three-input max.
+__device__ __forceinline__ float max32(const uint32_t* v) {
+  float m[4];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) m[i] = fmaxf(__uint_as_float(v[i]), __uint_as_float(v[8 + i]));
+  for (int i = 0; i < 4; ++i) m[i] = fmaxf(__uint_as_float(v[i]), __uint_as_float(v[4 + i]));
 #pragma unroll
-  for (int i = 16; i < 64; i += 16)
+  for (int i = 8; i < 32; i += 8)
 #pragma unroll
-    for (int c = 0; c < 8; ++c)
-      m[c] = fmax3(m[c], __uint_as_float(v[i + c]), __uint_as_float(v[i + 8 + c]));
-  return fmaxf(fmax3(m[0], m[1], m[2]), fmax3(fmax3(m[3], m[4], m[5]), m[6], m[7]));
+    for (int c = 0; c < 4; ++c)
+      m[c] = fmax3(m[c], __uint_as_float(v[i + c]), __uint_as_float(v[i + 4 + c]));
+  return fmax3(fmaxf(m[0], m[1]), m[2], m[3]);
 }
 
-// p = 2^(s * c - m) for 64 logits, packed as fp16 pairs into 32 words;
-// returns the fp32 sum of the p. The scale-and-subtract and the running sums
-// use paired fp32 arithmetic (four independent sum chains).
-__device__ __forceinline__ float exp_pack64(const uint32_t* v, float c, float negm,
+// p = 2^(s * c - m) for 32 logits, packed as fp16 pairs into 16 words;
+// returns the fp32 sum of the p (paired fp32 arithmetic, four sum chains).
+__device__ __forceinline__ float exp_pack32(const uint32_t* v, float c, float negm,
                                             uint32_t* pk) {
   const uint64_t c2 = f2_pack(c, c), m2 = f2_pack(negm, negm);
   uint64_t acc[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) acc[i] = 0ull;
 #pragma unroll
-  for (int u = 0; u < 64; u += 2) {
+  for (int u = 0; u < 32; u += 2) {
     const uint64_t y = f2_fma(f2_pack(__uint_as_float(v[u]), __uint_as_float(v[u + 1])), c2, m2);
     float y0, y1;
     f2_unpack(y, y0, y1);
@@ -182,12 +194,14 @@ __device__ __forceinline__ float exp_pack64(const uint32_t* v, float c, float ne
   return lo + hi;
 }
 
-// The ragged last key block: logits of keys past S become -inf (weight 0).
-__device__ __forceinline__ void mask_tail(uint32_t* v, uint32_t entry, int Nb, int last_valid) {
+// Keys [32 half, 32 half + 32) of a key block: in the ragged last block the
+// logits of keys past S become -inf (weight 0).
+__device__ __forceinline__ void mask_tail32(uint32_t* v, uint32_t entry, int half, int Nb,
+                                            int last_valid) {
   if (static_cast<int>(entry >> 2) == Nb - 1) {
 #pragma unroll
-    for (int u = 0; u < 64; ++u)
-      if (u >= last_valid) v[u] = __float_as_uint(-INFINITY);
+    for (int u = 0; u < 32; ++u)
+      if (u + 32 * half >= last_valid) v[u] = __float_as_uint(-INFINITY);
   }
 }
 
@@ -206,7 +220,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
-  const AbortSignal abort_sig{abort_flag, a.dev_status};
+  const AbortSignal abort_sig{abort_flag, a.grid_abort};
   const volatile int never_flag = 0;
   const AbortSignal drain_sig{&never_flag, nullptr};  // drains wait out their own limit
   volatile int* hdr = reinterpret_cast<volatile int*>(smem + L::kHdr);
@@ -214,6 +228,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   auto bar = [&](int i) { return sbase + L::kBar + 8u * static_cast<uint32_t>(i); };
   auto fail = [&](int site) {
     *abort_flag = 1;
+    if (a.grid_abort) *reinterpret_cast<volatile int*>(a.grid_abort) = 1;
     note_timeout(a.dev_status, site);
   };
 
@@ -231,13 +246,15 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     for (int i = 0; i < L::kNumBars; ++i) {
       uint32_t cnt = 1;
       if (i == L::bInfoEmpty || i == L::bInfoEmpty + 1) cnt = 2 + kSoftmaxThreads;
-      if (i >= L::bPFull && i < L::bPFull + kSBuf) cnt = kSoftmaxThreads;
+      if (i >= L::bPFull && i < L::bPFull + kSBuf) cnt = kSetThreads;
       if (i == L::bOFree) cnt = kSoftmaxThreads;
       mbar_init(bar(i), cnt);
     }
     *abort_flag = 0;
     fence_barrier_init();
   }
+  if (threadIdx.x < kSoftmaxThreads)   // no step published yet (index -1)
+    reinterpret_cast<uint64_t*>(smem + L::kHand)[threadIdx.x] = 0xffffffff00000000ull;
   if (warp == kMmaWarp) {
     tmem_alloc(sbase + L::kMisc, kTmemCols);
     tmem_relinquish();
@@ -261,8 +278,13 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     // Takes tiles in order from the global counter and writes each tile's
     // key walk (the rotated union of its two query blocks' key lists, with
     // a 2-bit membership mask per key block) into walk buffer it % 2.
+    // A route that breaks the CSR contract raises SA_DEV_BAD_ROUTE: a row
+    // whose span is not inside [0, nnz] or longer than Nb is skipped whole,
+    // an entry outside [0, Nb) is skipped, and a row that is not strictly
+    // ascending (a duplicate included) is attended as the set of its entries.
     uint32_t* bmA = reinterpret_cast<uint32_t*>(smem + L::kBits);
     uint32_t* bmB = bmA + kMaxNbAttn / 32;
+    const int nnz = a.row_ptr != nullptr ? a.row_ptr[a.nnz_row] : 0;
     for (int it = 0;; ++it) {
       const int x = it & 1;
       int tile = 0;
@@ -299,7 +321,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       }
       const bool has_qb1 = qb1 >= 0;
       // Union of the two query blocks' key lists with a 2-bit membership mask
-      // per key block (bit 0: block 2p lists it, bit 1: block 2p+1 does),
+      // per key block (bit 0: block qb0 lists it, bit 1: block qb1 does),
       // ascending but rotated to start at the tile's own diagonal block: the
       // row maxima usually sit near the diagonal, so taking it first keeps
       // later steps from raising the running max (each raise rescales O).
@@ -316,12 +338,21 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           if (half == 1 && !has_qb1) break;
           const int64_t r = (static_cast<int64_t>(b) * a.H + h) * Nb + (half ? qb1 : qb0);
           const int beg = a.row_ptr[r], end = a.row_ptr[r + 1];
-          if (beg < 0 || end < beg || end - beg > Nb) { bad = 1; continue; }
+          if (beg < 0 || end < beg || end - beg > Nb || end > nnz) { bad = 1; continue; }
           uint32_t* bm = half ? bmB : bmA;
-          for (int e = beg + lane; e < end; e += 32) {
-            const int j = a.col_idx[e];
-            if (j < 0 || j >= Nb) bad = 1;
-            else atomicOr(&bm[j >> 5], 1u << (j & 31));
+          int carry = INT_MIN;                 // the entry before this chunk
+          for (int e0 = beg; e0 < end; e0 += 32) {
+            const int e = e0 + lane;
+            const bool in = e < end;
+            const int j = in ? a.col_idx[e] : INT_MAX;
+            int prev = __shfl_up_sync(full, j, 1);
+            if (lane == 0) prev = carry;
+            if (in && prev >= j) bad = 1;      // not strictly ascending
+            if (in) {
+              if (j < 0 || j >= Nb) bad = 1;
+              else atomicOr(&bm[j >> 5], 1u << (j & 31));
+            }
+            carry = __shfl_sync(full, j, 31);
           }
         }
         __syncwarp();
@@ -406,34 +437,36 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             tma_load_4d(sbase + L::kQ + dh * L::kRegion + qh * 8192, &tm_q, bar(L::bQFull),
                         dh * 64, qh ? qrow1 : qrow0, h, b);
         const int n_steps = (n + 1) >> 1;
-        bool ok = true;
-        for (int t = 0; t < n_steps + 2 && ok; ++t) {
-          for (int kind = 0; kind < 2; ++kind) {       // 0: K(t), 1: V(t - 2)
-            const int js = kind == 0 ? t : t - 2;
-            if (js < 0 || js >= n_steps) continue;
-            const int st = c % KVST;
-            if (c >= KVST &&
-                !mbar_wait(bar(L::bKVEmpty + st), ((c / KVST) - 1) & 1, abort_sig)) {
-              fail(kSiteKVStage);
-              ok = false;
-              break;
-            }
-            const int nblk = (2 * js + 1 < n) ? 2 : 1;
-            mbar_arrive_expect_tx(bar(L::bKVFull + st), nblk * kBlock * D * 2);
-            ++issued[st];
-            const uint32_t dst = sbase + L::kKV + st * L::kStageBytes;
-            for (int kh = 0; kh < nblk; ++kh) {
-              const int jk = inf[2 * js + kh] >> 2;
-              if (kind == 0) {
-                for (int dh = 0; dh < D / 64; ++dh)
-                  tma_load_4d(dst + dh * L::kRegion + kh * 8192, &tm_k, bar(L::bKVFull + st),
-                              dh * 64, jk * kBlock, h, b);
-              } else {
-                tma_load_3d(dst + kh * L::kVHalf, &tm_vt, bar(L::bKVFull + st), jk * kBlock, 0, bh);
-              }
-            }
-            ++c;
+        // one ring item: K (kind 0) or V^T (kind 1) of step js
+        auto load_item = [&](int kind, int js) -> bool {
+          const int st = c % KVST;
+          if (c >= KVST && !mbar_wait(bar(L::bKVEmpty + st), ((c / KVST) - 1) & 1, abort_sig)) {
+            fail(kSiteKVStage);
+            return false;
           }
+          const int nblk = (2 * js + 1 < n) ? 2 : 1;
+          mbar_arrive_expect_tx(bar(L::bKVFull + st), nblk * kBlock * D * 2);
+          ++issued[st];
+          const uint32_t dst = sbase + L::kKV + st * L::kStageBytes;
+          for (int kh = 0; kh < nblk; ++kh) {
+            const int jk = inf[2 * js + kh] >> 2;
+            if (kind == 0) {
+              for (int dh = 0; dh < D / 64; ++dh)
+                tma_load_4d(dst + dh * L::kRegion + kh * 8192, &tm_k, bar(L::bKVFull + st),
+                            dh * 64, jk * kBlock, h, b);
+            } else {
+              tma_load_3d(dst + kh * L::kVHalf, &tm_vt, bar(L::bKVFull + st), jk * kBlock, 0, bh);
+            }
+          }
+          ++c;
+          return true;
+        };
+        bool ok = true;
+        if (n_steps > 0) ok = load_item(0, 0);
+        if (ok && n_steps > 1) ok = load_item(0, 1);
+        for (int j = 0; j < n_steps && ok; ++j) {
+          if (j + 2 < n_steps) ok = load_item(0, j + 2);
+          if (ok) ok = load_item(1, j);
         }
         if (!ok) break;
         mbar_arrive(bar(L::bInfoEmpty + x));
@@ -446,9 +479,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     regs_dec<kControlRegs>();
     // ------------------------------------------------------------------ MMA
     // The whole warp runs this loop in step (warp-uniform waits); elect.sync
-    // picks the lane that issues each batch of MMAs and each commit. Order per
-    // tile: QK(0), QK(1), then for each step j: QK(j+2) (if any), PV(j) --
-    // the same order in which the producer fills the ring.
+    // picks the lane that issues each batch of MMAs and each commit (lane 0
+    // of the converged warp, so every commit tracks every earlier MMA). Order
+    // per tile: QK(0), QK(1), then for each step j: QK(j+2) (if any), PV(j)
+    // -- the same order in which the producer fills the ring.
     constexpr uint32_t kIdQK128 = idesc_f16(BM, 128, 1);
     constexpr uint32_t kIdQK64 = idesc_f16(BM, 64, 1);
     constexpr uint32_t kIdPV = idesc_f16(BM, D, 0);
@@ -556,41 +590,65 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   } else {
     regs_inc<kSoftmaxRegs>();
     // ------------------------------------------------------------- softmax
+    const int sm = warp >> 2;                  // warpgroup: steps g with g % 2 == sm
     const int quarter = warp & 3;              // TMEM lane quarter
-    const int half = warp >> 2;                // key block of the step this thread takes
     const int r = quarter * 32 + lane;         // tile row == TMEM lane
     const int qh = r >> 6;                     // query block of this row (warp-uniform)
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    const uint32_t o_col = kColO + half * (D / 2);   // this thread's half of O's columns
     const uint32_t pair_bar = 1 + quarter;     // named barrier of warps quarter, quarter + 4
     const int last_valid = S - (Nb - 1) * kBlock;  // tokens in the last block
     const float cl2 = a.scale_log2;
-    float* xv = reinterpret_cast<float*>(smem + L::kXch);       // [2 slots][2 halves][BM]
-    int* xs = reinterpret_cast<int*>(smem + L::kXch) + 2 * 2 * BM;
+    float* xm = reinterpret_cast<float*>(smem + L::kXch);      // [2 slots][2 warpgroups][BM]
+    float* xl = xm + 2 * kSets * BM;
+    int* xs = reinterpret_cast<int*>(xl + 2 * kSets * BM);
+    // running-max handoff: (step index << 32) | max bits, one 64-bit word
+    // per row and warpgroup, written and read whole
+    volatile uint64_t* hand = reinterpret_cast<volatile uint64_t*>(smem + L::kHand);
+    volatile uint64_t* hand_mine = hand + sm * BM + r;
+    const volatile uint64_t* hand_theirs = hand + (sm ^ 1) * BM + r;
     int xc = 0;                                // exchanges so far (slot xc & 1)
-    // Swap a value and a stop bit with the other thread of this row. Both
-    // warps of a pair pass the same sequence of exchanges, and a stop from
-    // either ends both, so neither is ever left waiting at the pair barrier.
-    // Slots alternate: a slot is rewritten only after the next exchange,
-    // which the partner reaches after reading it.
-    auto pair_xchg = [&](float v, bool stop, float& other) -> bool {
+    // Swap (m, l) and a stop bit with the other warpgroup's thread of this
+    // row. Both threads pass the same sequence of exchanges (two per tile),
+    // and a stop from either ends both, so neither is ever left waiting at
+    // the pair barrier. Slots alternate: a slot is rewritten only after the
+    // next exchange, which the partner reaches after reading it.
+    auto pair_xchg = [&](float m, float l, bool stop, float& m_o, float& l_o) -> bool {
       const int sl = xc & 1;
       ++xc;
-      xv[(sl * 2 + half) * BM + r] = v;
-      xs[(sl * 2 + half) * BM + r] = stop ? 1 : 0;
+      const int mine = (sl * kSets + sm) * BM + r, theirs = (sl * kSets + (sm ^ 1)) * BM + r;
+      xm[mine] = m;
+      xl[mine] = l;
+      xs[mine] = stop ? 1 : 0;
       named_bar_sync(pair_bar, 64);
-      other = xv[(sl * 2 + (half ^ 1)) * BM + r];
-      return stop || xs[(sl * 2 + (half ^ 1)) * BM + r] != 0;
+      m_o = xm[theirs];
+      l_o = xl[theirs];
+      return stop || xs[theirs] != 0;
     };
-    int gs = 0;                                // this CTA's steps so far (all tiles)
-    bool ok = true;
+    // Waits (bounded, like every wait here) until the other warpgroup has
+    // published the running max after step g_prev for this warp's rows.
+    auto wait_handoff = [&](int g_prev, uint64_t& hv) -> bool {
+      hv = *hand_theirs;
+      if (__all_sync(full, static_cast<int>(hv >> 32) >= g_prev)) return true;
+      unsigned long long t0 = 0;
+      if (lane == 0) t0 = globaltimer();
+      for (uint32_t i = 1;; ++i) {
+        hv = *hand_theirs;
+        if (__all_sync(full, static_cast<int>(hv >> 32) >= g_prev)) return true;
+        if ((i & 63u) == 0u) {
+          int give_up = 0;
+          if (lane == 0) give_up = abort_sig.raised() || (globaltimer() - t0 > kWaitTimeoutNs);
+          if (__shfl_sync(full, give_up, 0)) return false;
+        }
+      }
+    };
+    int gs = 0;                                // steps of this CTA's earlier tiles
 
-    for (int it = 0; ok; ++it) {
+    for (int it = 0;; ++it) {
       const int x = it & 1;
       bool stop = !mbar_wait_warp(bar(L::bInfoFull + x), (it >> 1) & 1, abort_sig);
       if (stop && lane == 0) fail(kSiteInfo);
-      float unused;
-      if (pair_xchg(0.f, stop, unused)) break;
+      float u0, u1;
+      if (pair_xchg(0.f, 0.f, stop, u0, u1)) break;
       const volatile int* hd = hdr + 4 * x;
       const int n = hd[3];
       if (n < 0) break;
@@ -601,98 +659,149 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       const uint16_t* inf = info + x * kMaxNbAttn;
       const int n_steps = (n + 1) >> 1;
       const int t = qb * kBlock + (r & (kBlock - 1));   // query token (< 0: no block)
+      // m_run: the max this warpgroup's latest step of the tile used (the
+      // scale of l_run, its partial row sum)
       float m_run = -INFINITY, l_run = 0.f;
 
-      for (int j = 0; j < n_steps; ++j, ++gs) {
-        const int sb = gs % kSBuf;
+      for (int j = (gs ^ sm) & 1; j < n_steps; j += kSets) {
+        const int g = gs + j, sb = g % kSBuf;
         const uint32_t s_col = kColS + sb * 128;
-        stop = !mbar_wait_warp(bar(L::bSFull + sb), (gs / kSBuf) & 1, abort_sig);
-        if (stop && lane == 0) fail(kSiteSFull);
-        tc_fence_after();
-        const bool has = half == 0 || 2 * j + 1 < n;   // an odd walk's last step has one block
-        const uint32_t e = has ? inf[2 * j + half] : 0u;
-        const bool mem = has && ((e >> qh) & 1u);
-        uint32_t sr[64];
-        float mx = -INFINITY;
-        if (mem && !stop) {
-          tmem_ld32(lane_base + s_col + half * 64, sr);
-          tmem_ld32(lane_base + s_col + half * 64 + 32, sr + 32);
-          tmem_wait_ld();
-          reg_fence64(sr);
-          mask_tail(sr, e, Nb, last_valid);
-          mx = max64(sr);
-        }
-        float mo;
-        if (pair_xchg(mx, stop, mo)) {
-          ok = false;
+        if (!mbar_wait_warp(bar(L::bSFull + sb), (g / kSBuf) & 1, abort_sig)) {
+          if (lane == 0) fail(kSiteSFull);
+          stop = true;
           break;
         }
-        const float bmax = fmaxf(mx, mo) * cl2;  // the scale is positive: max commutes
-        float m_new = m_run;
-        if (bmax > m_run + kRescaleLog2) m_new = bmax;  // also the first finite block
-        const bool rescale = (m_new != m_run) && (m_run != -INFINITY);
-        const float alpha = rescale ? fast_exp2(m_run - m_new) : 1.f;
-        // P over this thread's 64 keys: 32 columns (two fp16 per column) at
-        // the start of its half of the consumed S columns.
+        tc_fence_after();
+        const bool two = 2 * j + 1 < n;             // an odd walk's last step has one block
+        const uint32_t e0 = inf[2 * j], e1 = two ? inf[2 * j + 1] : 0u;
+        const bool mem0 = (e0 >> qh) & 1u, mem1 = two && ((e1 >> qh) & 1u);
+        uint32_t sr[128];
+        if (mem0) {
+          tmem_ld32(lane_base + s_col, sr);
+          tmem_ld32(lane_base + s_col + 32, sr + 32);
+        }
+        if (mem1) {
+          tmem_ld32(lane_base + s_col + 64, sr + 64);
+          tmem_ld32(lane_base + s_col + 96, sr + 96);
+        }
+        float mx = -INFINITY;
+        if (mem0 || mem1) {
+          tmem_wait_ld();
+          if (mem0) {
+            reg_fence32(sr);
+            reg_fence32(sr + 32);
+            mask_tail32(sr, e0, 0, Nb, last_valid);
+            mask_tail32(sr + 32, e0, 1, Nb, last_valid);
+            mx = fmaxf(max32(sr), max32(sr + 32));
+          }
+          if (mem1) {
+            reg_fence32(sr + 64);
+            reg_fence32(sr + 96);
+            mask_tail32(sr + 64, e1, 0, Nb, last_valid);
+            mask_tail32(sr + 96, e1, 1, Nb, last_valid);
+            mx = fmaxf(mx, fmaxf(max32(sr + 64), max32(sr + 96)));
+          }
+        }
+        const float bmax = mx * cl2;             // the scale is positive: max commutes
+        // the running max after step g - 1 (none before the tile's first step)
+        float m_prev = -INFINITY;
+        if (j > 0) {
+          uint64_t hv;
+          if (!wait_handoff(g - 1, hv)) {
+            if (lane == 0) fail(kSiteHandoff);
+            stop = true;
+            break;
+          }
+          m_prev = __uint_as_float(static_cast<uint32_t>(hv));
+        }
+        float m_new = m_prev;
+        if (bmax > m_prev + kRescaleLog2) m_new = bmax;  // also the first finite block
+        *hand_mine = (static_cast<uint64_t>(static_cast<uint32_t>(g)) << 32) | __float_as_uint(m_new);
+        const bool raised = (m_new != m_prev) && (m_prev != -INFINITY);
+        if (__any_sync(full, raised)) {
+          // O holds this tile's PVs of the steps before g; the last of them,
+          // PV(g - 1), must be done before O is rescaled (PV(g) waits for this
+          // step's p_full, so no later PV can be running). A parity wait needs
+          // the barrier within one phase of the one waited for: S(g) is
+          // written after PV(g - 3) in the tensor pipe's order, so on the
+          // barrier of g - 1's parity the phase before it is done.
+          if (!mbar_wait_warp(bar(L::bPVDone + ((g - 1) & 1)), ((g - 1) >> 1) & 1, abort_sig)) {
+            if (lane == 0) fail(kSitePVDone);
+            stop = true;
+            break;
+          }
+          tc_fence_after();
+          const float alpha = raised ? fast_exp2(m_prev - m_new) : 1.f;
+#pragma unroll 1
+          for (int cc = 0; cc < D / 32; ++cc) {
+            uint32_t o[32];
+            tmem_ld32(lane_base + kColO + 32 * cc, o);
+            tmem_wait_ld();
+            reg_fence32(o);
+#pragma unroll
+            for (int u = 0; u < 32; ++u) o[u] = __float_as_uint(__uint_as_float(o[u]) * alpha);
+            tmem_st32(lane_base + kColO + 32 * cc, o);
+          }
+        }
+        // P over the step's keys: 32 columns (two fp16 per column) per key
+        // block at the start of the consumed S columns.
         float rs = 0.f;
-        if (has) {
+        {
           uint32_t pk[32];
-          if (mem) rs = exp_pack64(sr, cl2, -m_new, pk);
-          else {
+          if (mem0) {
+            rs = exp_pack32(sr, cl2, -m_new, pk);
+            rs += exp_pack32(sr + 32, cl2, -m_new, pk + 16);
+          } else {
 #pragma unroll
             for (int u = 0; u < 32; ++u) pk[u] = 0u;
           }
-          tmem_st32(lane_base + s_col + half * 32, pk);
+          tmem_st32(lane_base + s_col, pk);
         }
-        l_run = l_run * alpha + rs;
-        m_run = m_new;
-        if (__any_sync(full, rescale)) {
-          // O holds this tile's PVs of the steps before j; the last of them,
-          // PV number gs - 1, must be done before O is rescaled (PV(j) waits
-          // for this step's p_full, so no later PV can be running). A parity
-          // wait needs the barrier within one phase of the one waited for:
-          // S(j) is written after PV(gs - 3) in the tensor pipe's order, so
-          // on the barrier of gs - 1's parity the phase before it is done.
-          if (!mbar_wait_warp(bar(L::bPVDone + ((gs - 1) & 1)), ((gs - 1) >> 1) & 1, abort_sig)) {
-            if (lane == 0) fail(kSitePVDone);
+        if (two) {
+          uint32_t pk[32];
+          if (mem1) {
+            rs += exp_pack32(sr + 64, cl2, -m_new, pk);
+            rs += exp_pack32(sr + 96, cl2, -m_new, pk + 16);
           } else {
-            tc_fence_after();
-#pragma unroll 1
-            for (int cc = 0; cc < D / 64; ++cc) {
-              uint32_t o[32];
-              tmem_ld32(lane_base + o_col + 32 * cc, o);
-              tmem_wait_ld();
-              reg_fence32(o);
 #pragma unroll
-              for (int u = 0; u < 32; ++u) o[u] = __float_as_uint(__uint_as_float(o[u]) * alpha);
-              tmem_st32(lane_base + o_col + 32 * cc, o);
-            }
+            for (int u = 0; u < 32; ++u) pk[u] = 0u;
           }
+          tmem_st32(lane_base + s_col + 32, pk);
         }
+        // this warpgroup's sum, carried to the new max
+        l_run = (l_run > 0.f ? l_run * fast_exp2(m_run - m_new) : 0.f) + rs;
+        m_run = m_new;
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(bar(L::bPFull + sb));
       }
-      if (!ok) break;
-      mbar_arrive(bar(L::bInfoEmpty + x));     // done with this walk
+      gs += n_steps;
+      if (!stop) mbar_arrive(bar(L::bInfoEmpty + x));     // done with this walk
 
       // -------------------------------------------------------- epilogue
-      // Both threads of the row add their partial sums; each writes its half
-      // of the output columns once every PV of the tile is done.
-      stop = !mbar_wait_warp(bar(L::bTileDone), it & 1, abort_sig);
-      if (stop && lane == 0) fail(kSiteFin);
-      float l_other;
-      if (pair_xchg(l_run, stop, l_other)) break;
+      // The two threads of the row add their partial sums (each carried to
+      // the later max); each writes half of the output columns once every
+      // PV of the tile is done.
+      if (!stop) {
+        stop = !mbar_wait_warp(bar(L::bTileDone), it & 1, abort_sig);
+        if (stop && lane == 0) fail(kSiteFin);
+      }
+      float m_oth, l_oth;
+      if (pair_xchg(m_run, l_run, stop, m_oth, l_oth)) break;
       tc_fence_after();
-      const float l_tot = l_run + l_other;
+      // O is scaled to the tile's last max, the larger of the two
+      const float m_tot = fmaxf(m_run, m_oth);
+      const float f_own = l_run > 0.f ? fast_exp2(m_run - m_tot) : 0.f;
+      const float f_oth = l_oth > 0.f ? fast_exp2(m_oth - m_tot) : 0.f;
+      const float l_tot = l_run * f_own + l_oth * f_oth;
       const float inv_l = l_tot > 0.f ? 1.f / l_tot : 0.f;
       const bool row_ok = qb >= 0 && t < S;
-      uint16_t* orow = a.o + b * a.os[0] + static_cast<int64_t>(t) * a.os[1] + h * a.os[2] +
-                       half * (D / 2);
+      const int c0 = sm * (D / 2);              // this thread's output columns
+      uint16_t* orow = a.o + b * a.os[0] + static_cast<int64_t>(t) * a.os[1] + h * a.os[2] + c0;
 #pragma unroll
       for (int cc = 0; cc < D / 64; ++cc) {
         uint32_t ov[32];
-        tmem_ld32(lane_base + o_col + 32 * cc, ov);
+        tmem_ld32(lane_base + kColO + c0 + 32 * cc, ov);
         tmem_wait_ld();
         reg_fence32(ov);
         if (row_ok) {
@@ -716,8 +825,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       }
       tc_fence_before();
       mbar_arrive(bar(L::bOFree));             // O read
-      if (row_ok && half == 0 && a.lse) {
-        const float lse = l_tot > 0.f ? m_run * 0.69314718055994531f + logf(l_tot) : -INFINITY;
+      if (row_ok && sm == 0 && a.lse) {
+        const float lse = l_tot > 0.f ? m_tot * 0.69314718055994531f + logf(l_tot) : -INFINITY;
         a.lse[(static_cast<int64_t>(b) * a.H + h) * S + t] = lse;
       }
     }

@@ -81,9 +81,9 @@ __device__ __forceinline__ uint64_t edge_key(uint32_t w, int lo, int d) {
 // CSR contract count as empty (the attention planner reports them) and
 // entries outside [0, Nb) are skipped.
 __device__ void row_bits_checked(const int32_t* row_ptr, const int32_t* col_idx, int64_t r,
-                                 int Nb, uint32_t* bits, int lane) {
+                                 int Nb, int nnz, uint32_t* bits, int lane) {
   const int beg = row_ptr[r], end = row_ptr[r + 1];
-  if (beg < 0 || end < beg || end - beg > Nb) return;
+  if (beg < 0 || end < beg || end - beg > Nb || end > nnz) return;
   for (int e = beg + lane; e < end; e += 32) {
     const int j = col_idx[e];
     if (j >= 0 && j < Nb) atomicOr(&bits[j >> 5], 1u << (j & 31));
@@ -105,7 +105,8 @@ __global__ void __launch_bounds__(kRankThreads) pair_rank_kernel(PairArgs a) {
   for (int i = threadIdx.x; i <= rows; i += kRankThreads) rp[i] = a.row_ptr[row0 + i];
   for (int i = threadIdx.x; i < rows * ld; i += kRankThreads) bits[i] = 0u;
   __syncthreads();
-  bool valid = rp[0] >= 0;
+  const int nnz = a.row_ptr[a.nnz_row];   // entries of the whole route
+  bool valid = rp[0] >= 0 && rp[rows] <= nnz;
   for (int i = threadIdx.x; i < rows; i += kRankThreads)
     valid = valid && rp[i + 1] >= rp[i] && rp[i + 1] - rp[i] <= Nb;
   if (__syncthreads_and(valid)) {
@@ -131,7 +132,7 @@ __global__ void __launch_bounds__(kRankThreads) pair_rank_kernel(PairArgs a) {
     }
   } else {
     for (int i = warp; i < rows; i += kRankThreads / 32)
-      row_bits_checked(a.row_ptr, a.col_idx, row0 + i, Nb, bits + i * ld, lane);
+      row_bits_checked(a.row_ptr, a.col_idx, row0 + i, Nb, nnz, bits + i * ld, lane);
   }
   __syncthreads();
 

@@ -14,14 +14,15 @@ namespace sa {
 constexpr unsigned long long kWaitTimeoutNs = 250000000ull;  // 250 ms
 
 // Where a waiting thread learns that it should stop: a flag of its own CTA,
-// and (optionally) the caller's status word, whose timeout bit any CTA of the
-// launch may set, so one stuck CTA does not make every other CTA wait out its
-// own limit.
+// and (optionally) a word of the launch, zeroed before it, that any CTA sets
+// when one of its waits gives up, so one stuck CTA does not make every other
+// CTA wait out its own limit. The launch word is never the caller's status
+// word: a timeout left there by an earlier call must not abort this one.
 struct AbortSignal {
   const volatile int* cta;
   const volatile int* grid;  // may be null
   __device__ __forceinline__ bool raised() const {
-    return *cta != 0 || (grid != nullptr && (*grid & 2) != 0);
+    return *cta != 0 || (grid != nullptr && *grid != 0);
   }
 };
 

@@ -172,6 +172,7 @@ sa_status attn_prepare_launch(const sa_params* p, const void* v, const int32_t* 
     pa.pairs = reinterpret_cast<uint32_t*>(wsb + L.pairs);
     pa.Nb = Nb;
     pa.n_pairs = (Nb + 1) / 2;
+    pa.nnz_row = static_cast<int64_t>(p->B) * p->H * Nb;
     if (launch_pair(pa, p->B * p->H, st) != cudaSuccess) return SA_ERR_CUDA;
   }
   return SA_OK;
@@ -205,8 +206,11 @@ sa_status attn_run_launch(const sa_params* p, const void* q, const void* k,
   a.n_pairs = (Nb + 1) / 2;
   a.scale_log2 = static_cast<float>(scale64_of(p) * 1.4426950408889634);
   a.n_tiles = p->B * p->H * a.n_pairs;
+  a.nnz_row = static_cast<int64_t>(p->B) * p->H * Nb;
+  // the tile counter and the launch's abort word, zeroed together
   a.tile_counter = reinterpret_cast<int*>(wsb + L.counter);
-  if (cudaMemsetAsync(a.tile_counter, 0, sizeof(int), st) != cudaSuccess) return SA_ERR_CUDA;
+  a.grid_abort = a.tile_counter + 1;
+  if (cudaMemsetAsync(a.tile_counter, 0, 2 * sizeof(int), st) != cudaSuccess) return SA_ERR_CUDA;
   return from_cuda(launch_attn(p->D, maps, a, st));
 }
 

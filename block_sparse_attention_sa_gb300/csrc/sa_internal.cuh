@@ -83,6 +83,7 @@ struct PairArgs {
   const int32_t* col_idx;
   int16_t* cand;           // [B*H*Nb][2 kPairWindow] candidates of each block, best first
   uint32_t* pairs;         // [B*H][n_pairs] a | b << 16 (a < b; b = 0xffff: a alone)
+  int64_t nnz_row;         // B*H*Nb: row_ptr[nnz_row] is the route's entry count
   int Nb, n_pairs;
 };
 
@@ -100,6 +101,8 @@ struct AttnArgs {
   int B, S, H, Nb, n_pairs;
   float scale_log2;        // softmax_scale * log2(e)
   int* tile_counter;       // zeroed before the launch; tiles are taken in order
+  int* grid_abort;         // zeroed before the launch; set by a CTA whose wait gave up
+  int64_t nnz_row;         // B*H*Nb: row_ptr[nnz_row] is the route's entry count
   int n_tiles;             // B * H * n_pairs
 };
 

@@ -51,9 +51,14 @@ sa_status scratch_address(void** out) {
 extern "C" sa_status sa_route_static(const sa_params* p, const void* q, const void* k,
                                      int32_t* row_ptr, int32_t* col_idx, int64_t col_cap,
                                      int32_t* dev_status, void* stream) {
+  // Arguments first, in sa_route's order, then the capacity: a call that is
+  // wrong in both ways reports the argument, as sa_route would.
   const size_t need = sa_route_workspace_bytes(p);
   if (need == 0)  // invalid parameters: let sa_route name the problem
     return sa_route(p, q, k, row_ptr, col_idx, col_cap, nullptr, 0, dev_status, stream);
+  if (!q || !k || !row_ptr || !col_idx || col_cap < 0) return SA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(q) & 15u) != 0 || (reinterpret_cast<uintptr_t>(k) & 15u) != 0)
+    return SA_ERR_INVALID_ARG;
   if (need > SA_ROUTE_STATIC_WS_BYTES) return SA_ERR_CAPACITY;
   void* ws = nullptr;
   const sa_status s = scratch_address(&ws);

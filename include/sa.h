@@ -55,9 +55,9 @@ enum {
                                CSR is truncated (row_ptr is still exact)      */
   SA_DEV_TIMEOUT = 1 << 1,  /* a bounded pipeline wait gave up; the output of
                                the affected tiles is undefined                */
-  SA_DEV_BAD_ROUTE = 1 << 2,/* sa_attn_sparse met a row that is not ascending,
-                               has an index outside [0, Nb) or a bad row_ptr;
-                               that row is skipped                            */
+  SA_DEV_BAD_ROUTE = 1 << 2,/* sa_attn_sparse met a CSR that breaks its
+                               contract (see sa_attn_sparse for what is then
+                               attended)                                      */
   SA_DEV_RANGE = 1 << 3     /* a V value does not fit fp16 (|v| > 65504); the
                                P.V product runs in fp16, see sa_attn_sparse    */
 };
@@ -173,8 +173,10 @@ sa_status sa_route(const sa_params* p, const void* q, const void* k,
  *
  * Limits and behaviour:
  *  - Shapes whose sa_route_workspace_bytes(p) exceeds SA_ROUTE_STATIC_WS_BYTES
- *    are rejected with SA_ERR_CAPACITY before anything is launched (for
- *    example S = 38,247 fits up to 8 heads of D = 128, S = 8,192 up to 64).
+ *    are rejected with SA_ERR_CAPACITY before anything is launched. With
+ *    D = 128 and 64-token query blocks the limit is 9 heads at S = 38,247,
+ *    72 at S = 8,192 and 1 at S = 112,640 (15, 101 and 3 heads with
+ *    q_block = 128); sa_route_workspace_bytes gives the need of any shape.
  *  - The first call on each device, made with that device current, looks up
  *    the array's device address and caches it; make that first call before
  *    any stream capture.
@@ -240,7 +242,9 @@ sa_status sa_route_pooled(const sa_params* p, int32_t* row_ptr, int32_t* col_idx
 size_t sa_attn_workspace_bytes(const sa_params* p);
 
 /*
- * sa_attn_sparse -- block-sparse attention forward over a route.
+ * sa_attn_sparse -- block-sparse attention forward over a route: only the
+ * routed (query block, key block) pairs are computed (MiniAcc blog, "What is
+ * Sol attention?"), each exactly (exact softmax over the selected keys).
  *
  * For every query token t of block i (head h, batch b), over the valid key
  * tokens u of the key blocks listed for row (b, h, i):
@@ -255,9 +259,16 @@ size_t sa_attn_workspace_bytes(const sa_params* p);
  * bf16. |v| must be <= 65504 (else SA_DEV_RANGE).
  *
  * q, k, v    device bf16 [B, S, H, D] (strides in p); not modified.
- * row_ptr,   device int32 CSR as written by sa_route (ascending, unique
- * col_idx    entries in [0, Nb)); rows that break this raise SA_DEV_BAD_ROUTE
- *            and are skipped.
+ * row_ptr,   device int32 CSR as written by sa_route: row_ptr[B*H*Nb] = nnz
+ * col_idx    entries in col_idx (which must hold at least that many), each
+ *            row strictly ascending with entries in [0, Nb). A CSR that
+ *            breaks this raises SA_DEV_BAD_ROUTE and is attended as follows:
+ *            a row whose span [row_ptr[r], row_ptr[r+1]) does not lie inside
+ *            [0, nnz] or is longer than Nb is skipped whole (its query rows
+ *            give o = 0, lse = -inf; col_idx is not read for it); entries
+ *            outside [0, Nb) are skipped; a row that is not strictly
+ *            ascending (a repeated entry included) is attended as the set of
+ *            its entries. Nothing is read outside col_idx[0, nnz).
  * o          device bf16 [B, S, H, D] (o_stride); rows >= S are not written.
  * lse        device fp32 [B, H, S] (natural log), or NULL.
  * workspace  device scratch of sa_attn_workspace_bytes(p) bytes, 256-byte

@@ -220,3 +220,18 @@ def test_prepare_and_run_check_their_own_arguments(sa):
     assert L.sa_attn_run(ctypes.byref(p), None, a, a, a, a, None, a, big, None, None) == 1
     assert L.sa_attn_run(ctypes.byref(p), a, a, a, a, None, None, a, big, None, None) == 1
     assert L.sa_attn_run(ctypes.byref(p), a, a, a, a, a, None, a, 1024, None, None) == 3
+
+
+@pytest.mark.parametrize("S,q_block,max_heads", [(38247, 0, 9), (8192, 0, 72), (112640, 0, 1),
+                                                 (38247, 128, 15), (8192, 128, 101),
+                                                 (112640, 128, 3)])
+def test_static_route_limits_stated_in_the_header(sa, S, q_block, max_heads):
+    # the largest head counts sa.h states for sa_route_static's scratch array
+    L = sa.load_library()
+
+    def need(H):
+        p = params(sa, S=S, H=H, P=0)
+        p.q_block = q_block
+        return L.sa_route_workspace_bytes(ctypes.byref(p))
+
+    assert need(max_heads) <= sa.SA_ROUTE_STATIC_WS_BYTES < need(max_heads + 1)

@@ -242,6 +242,47 @@ def test_bad_route_entries_are_reported_and_skipped(sa):
     assert l2 <= L2_TOL and mx <= MAXABS_TOL
 
 
+def clean_csr(rp, ci, Nb):
+    """The route sa_attn_sparse attends for a CSR that breaks the contract: a
+    row whose span is not inside [0, row_ptr[-1]] or is longer than Nb is
+    empty; otherwise the row is the set of its entries inside [0, Nb)."""
+    nnz = int(rp[-1])
+    rows = []
+    for r in range(len(rp) - 1):
+        beg, end = int(rp[r]), int(rp[r + 1])
+        if beg < 0 or end < beg or end - beg > Nb or end > nnz:
+            rows.append([])
+        else:
+            rows.append(sorted({int(j) for j in ci[beg:end] if 0 <= j < Nb}))
+    out_rp = np.cumsum([0] + [len(x) for x in rows])
+    out_ci = np.array([j for x in rows for j in x], dtype=np.int64)
+    return out_rp, out_ci
+
+
+# Each case breaks the CSR contract in one way; the kernel reports it and
+# attends the cleaned route (S = 256: four key blocks).
+CORRUPT_CSR = {
+    "descending_row": ([0, 3, 4, 5, 6], [2, 1, 0, 1, 2, 3]),
+    "duplicate_column": ([0, 3, 4, 5, 6], [0, 1, 1, 1, 2, 3]),
+    "decreasing_row_ptr": ([0, 2, 1, 3, 4], [0, 1, 2, 3]),
+    "span_past_the_route": ([0, 6, 2, 3, 4], [0, 1, 2, 3]),
+}
+
+
+@pytest.mark.parametrize("case", sorted(CORRUPT_CSR))
+def test_corrupt_csr_is_reported_and_the_cleaned_route_attended(sa, case):
+    S, H, D = 256, 1, 64
+    q, k, v = sa_inputs.random_small(S, H, D, seed=41)
+    rp, ci = (np.array(x) for x in CORRUPT_CSR[case])
+    o, lse, st = gpu_attn(sa, q, k, v, rp, ci)
+    assert st & sa.SA_DEV_BAD_ROUTE
+    good_rp, good_ci = clean_csr(rp, ci, 4)
+    o_ref, lse_ref = oracle.attn_ref(q, k, v, good_rp, good_ci)
+    l2, mx, _ = out_errors(o, o_ref)
+    assert l2 <= L2_TOL and mx <= MAXABS_TOL
+    assert lse_ok(lse, lse_ref)
+
+
 def test_v_outside_fp16_range_is_reported(sa):
     q, k, v = sa_inputs.random_small(128, 1, 64, seed=3)
     v[0, 5, 0, 3] = 1.0e5
@@ -391,6 +432,28 @@ def test_bounded_wait_reports_timeout_and_the_context_survives(sa):
     cfg, q, k, v = sa_inputs.make_inputs("tiny")
     ref, rp, ci = check_route(sa, q, k, cfg.P, cfg.tau)
     check_attn_full(sa, q, k, v, rp, ci[:rp[-1]])
+
+
+def test_a_timeout_left_in_the_status_word_does_not_abort_later_calls(sa):
+    # the status word accumulates bits across calls: after a timeout was
+    # reported into it, later calls that share it still run to completion
+    L = sa.load_library()
+    st = new_status()
+    assert L.sa_check_wait_timeout(st.data_ptr(), torch.cuda.current_stream().cuda_stream) == 0
+    torch.cuda.synchronize()
+    assert int(st.item()) & sa.SA_DEV_TIMEOUT
+    cfg, q, k, v = sa_inputs.make_inputs("mid")
+    qd, kd, vd = dev(q, k, v)
+    rp, ci = sa.sa_route(qd, kd, cfg.P, cfg.tau, dev_status=st)
+    o, lse = sa.sa_attn_sparse(qd, kd, vd, rp, ci, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == sa.SA_DEV_TIMEOUT          # nothing new was reported
+    rp_n = to_np(rp).astype(np.int64)
+    ci_n = to_np(ci).astype(np.int64)[: rp_n[-1]]
+    o_ref, lse_ref = oracle.attn_ref(q, k, v, rp_n, ci_n)
+    l2, mx, _ = out_errors(to_np(o), o_ref)
+    assert l2 <= L2_TOL and mx <= MAXABS_TOL
+    assert lse_ok(to_np(lse), lse_ref)
 
 
 @pytest.mark.parametrize("name,q_block", [("tiny", 64), ("mid", 64), ("mid", 128)])

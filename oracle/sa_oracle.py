@@ -75,6 +75,21 @@ kernel). The page names the two operations only; the reading used here:
     schemes differ only in the tables.
 11. The router then pools the rounded (bf16) outputs, as in step 3.
 
+8-bit score computation (MiniAcc blog, "What is SageAttention?": the
+attention's score computation runs in 8-bit arithmetic instead of 16-bit;
+the page names no format or scaling; the reading used here, for FP8 e4m3,
+the 8-bit format GB300's tensor cores run fastest):
+
+12. Q and K are quantised per (batch, head, 64-token block): the block's
+    scale is 2^e with e the smallest integer such that amax / 2^e <= 448
+    (amax = the largest |x| over the block's valid tokens and all D; e = 0
+    for an all-zero block), and every x / 2^e is rounded to the nearest e4m3
+    value, ties to even (bias 7, three mantissa bits, subnormals below 2^-6,
+    largest finite value 448). Power-of-two scales keep x / 2^e exact, so the
+    rounding is the only approximation.
+13. Attention is step 7 with the logits of the dequantised Q and K
+    (code * 2^e); V, the softmax and the route are unchanged.
+
 The parity of a Sol "correction term" for skipped pairs (MiniAcc blog, same
 section) is not pinned: the pages give no formula and it is not applied.
 """
@@ -413,4 +428,115 @@ def qk_prologue_ref(x, gamma: Optional[np.ndarray], eps: float,
     out = np.empty_like(y)
     out[..., 0::2] = a * c - b * s_
     out[..., 1::2] = a * s_ + b * c
+    return out
+
+
+# ------------------------------------------------------------------ FP8 --
+
+E4M3_MAX = 448.0
+
+
+def e4m3_decode(code: int) -> float:
+    """The value of an e4m3 byte (step 12's format): sign bit, four exponent
+    bits with bias 7, three mantissa bits; exponent field 0 is subnormal
+    (m/8 * 2^-6); the all-ones pattern S.1111.111 is NaN (no infinities)."""
+    code = int(code) & 0xFF
+    sign = -1.0 if code & 0x80 else 1.0
+    ef, m = (code >> 3) & 0xF, code & 0x7
+    if ef == 0xF and m == 0x7:
+        return float("nan")
+    if ef == 0:
+        return sign * (m / 8.0) * 2.0 ** -6
+    return sign * (1.0 + m / 8.0) * 2.0 ** (ef - 7)
+
+
+def e4m3_round(x) -> np.ndarray:
+    """Step 12: round fp64 values with |x| <= 448 to the nearest e4m3 value,
+    ties to even. The spacing of e4m3 values in the binade [2^E, 2^(E+1)) is
+    2^(E-3), and 2^-9 below 2^-6 (the subnormals share the first normal
+    binade's spacing)."""
+    x = np.asarray(x, dtype=np.float64)
+    ax = np.abs(x)
+    _, k = np.frexp(np.where(ax > 0, ax, 1.0))       # ax = f 2^k, f in [0.5, 1)
+    E = np.maximum(k - 1, -6)                        # binade exponent, subnormals at -6
+    ulp = np.ldexp(1.0, (E - 3).astype(np.int64))
+    return np.round(x / ulp) * ulp                   # numpy rounds half to even
+
+
+def e4m3_encode(v) -> np.ndarray:
+    """The e4m3 byte of values already on the e4m3 grid (inverse of
+    e4m3_decode for finite values; -0 is encoded as +0)."""
+    v = np.asarray(v, dtype=np.float64)
+    av = np.abs(v)
+    _, k = np.frexp(np.where(av > 0, av, 1.0))
+    E = k - 1
+    sub = av < 2.0 ** -6
+    ef = np.where(sub, 0, E + 7)
+    m = np.where(sub, av / 2.0 ** -9, (av / np.ldexp(1.0, E.astype(np.int64)) - 1.0) * 8.0)
+    code = (ef.astype(np.int64) << 3) | np.rint(m).astype(np.int64)
+    code = np.where(av == 0, 0, code)
+    return (code | np.where(v < 0, 0x80, 0)).astype(np.uint8)
+
+
+def fp8_block_exponent(amax: float) -> int:
+    """Step 12: the smallest integer e with amax / 2^e <= 448 (0 for amax = 0).
+    With amax = f 2^k, f in [0.5, 1) and 448 = 0.875 * 2^9: e = k - 9, plus
+    one when f > 0.875."""
+    if amax == 0:
+        return 0
+    f, k = math.frexp(float(amax))
+    return int(k - 9 + (1 if f > 0.875 else 0))
+
+
+def quantize_qk_ref(x, heads: Optional[Sequence[int]] = None, block: int = BLOCK):
+    """Step 12 for a [B, S, H, D] tensor: returns (codes uint8 [B, S, Hs, D],
+    exponents int [B, Hs, Nb], dequantised values fp64 [B, S, Hs, D]) for the
+    heads in ``heads`` (all heads if None, in that order)."""
+    B, S, H, D = x.shape
+    heads = list(range(H)) if heads is None else list(heads)
+    Nb = num_blocks(S, block)
+    codes = np.zeros((B, S, len(heads), D), dtype=np.uint8)
+    exps = np.zeros((B, len(heads), Nb), dtype=np.int64)
+    deq = np.zeros((B, S, len(heads), D), dtype=np.float64)
+    for b in range(B):
+        for hi, h in enumerate(heads):
+            xf = _head_f64(x, b, h)
+            for j in range(Nb):
+                t0, t1 = j * block, min(S, j * block + block)
+                blk = xf[t0:t1]
+                e = fp8_block_exponent(np.abs(blk).max())
+                grid = e4m3_round(blk / 2.0 ** e)
+                exps[b, hi, j] = e
+                codes[b, t0:t1, hi, :] = e4m3_encode(grid)
+                deq[b, t0:t1, hi, :] = grid * 2.0 ** e
+    return codes, exps, deq
+
+
+def attn_fp8_ref(q, k, v, row_ptr: np.ndarray, col_idx: np.ndarray,
+                 scale: Optional[float] = None,
+                 items: Optional[Iterable[Tuple[int, int, int]]] = None,
+                 block: int = BLOCK):
+    """Step 13: step 7 over a CSR route with the logits of the dequantised Q
+    and K of step 12 (V unchanged). With ``items`` only their heads are
+    quantised; returns what attn_ref returns."""
+    B, S, H, D = q.shape
+    scale = 1.0 / math.sqrt(D) if not scale else scale
+    heads = sorted({h for (_, h, _) in items}) if items is not None else list(range(H))
+    _, _, qd = quantize_qk_ref(q, heads, block)
+    _, _, kd = quantize_qk_ref(k, heads, block)
+    qf = np.zeros((B, S, H, D)) if items is None else None
+    if items is None:
+        kf = np.zeros((B, S, H, D))
+        qf[:, :, heads, :] = qd
+        kf[:, :, heads, :] = kd
+        return attn_ref(qf, kf, v, row_ptr, col_idx, scale=scale, block=block)
+    Nb = num_blocks(S, block)
+    out = {}
+    for (b, h, i) in items:
+        hi = heads.index(h)
+        vf = _head_f64(v, b, h)[None, :, None, :]
+        r = (b * H + h) * Nb + i
+        blocks = [int(c) for c in col_idx[row_ptr[r]:row_ptr[r + 1]]]
+        out[(b, h, i)] = attend_rows(qd[b:b + 1, :, hi:hi + 1, :], kd[b:b + 1, :, hi:hi + 1, :],
+                                     vf, 0, 0, i, blocks, scale, block)
     return out

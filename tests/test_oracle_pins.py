@@ -541,3 +541,116 @@ def test_prologue_rope_scores_depend_on_relative_position():
     # tables are fp32, so equal up to their rounding
     assert abs(score(10, 3) - score(200, 193)) < 1e-4 * abs(score(10, 3)) + 1e-4
     assert abs(score(10, 3) - score(10, 40)) > 1e-3
+
+
+# ----------------------------------------------- 8-bit scores (FP8 e4m3) --
+
+def test_e4m3_decode_hand_values():
+    # bytes worked out from the format: sign, 4 exponent bits (bias 7), 3 mantissa bits
+    cases = {0x00: 0.0, 0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9, 0x08: 2.0 ** -6,
+             0x38: 1.0, 0x39: 1.125, 0x40: 2.0, 0x7E: 448.0, 0xB8: -1.0, 0xFE: -448.0}
+    for code, val in cases.items():
+        assert oracle.e4m3_decode(code) == val, hex(code)
+    assert math.isnan(oracle.e4m3_decode(0x7F)) and math.isnan(oracle.e4m3_decode(0xFF))
+
+
+def test_e4m3_round_hand_values():
+    # ties go to the even mantissa; subnormals are spaced 2^-9
+    x = [1.0625, 1.1875, 3 * 2.0 ** -10, 2.0 ** -10, 440.0, 447.0, 0.3, -1.0625, 1.9375]
+    want = [1.0, 1.25, 2.0 ** -8, 0.0, 448.0, 448.0, 0.3125, -1.0, 2.0]
+    assert oracle.e4m3_round(x).tolist() == want
+
+
+def test_e4m3_round_is_the_nearest_value_by_brute_force():
+    # against a search over every finite e4m3 value; ties take the even code
+    codes = [c for c in range(256) if not math.isnan(oracle.e4m3_decode(c))]
+    vals = np.array([oracle.e4m3_decode(c) for c in codes])
+    rng = np.random.default_rng(5)
+    x = np.concatenate([rng.uniform(-448, 448, 3000), rng.normal(0, 1, 3000),
+                        rng.normal(0, 2.0 ** -7, 2000), vals, (vals[:-1] + vals[1:]) / 2])
+    x = x[np.abs(x) <= 448]
+    got = oracle.e4m3_round(x)
+    for xi, gi in zip(x, got):
+        d = np.abs(vals - xi)
+        near = vals[d == d.min()]
+        if len(set(near.tolist()) - {0.0, -0.0}) > 1 or (len(near) > 1 and 0.0 not in near):
+            # a tie: the value whose code has an even mantissa
+            even = [v for v in near if (int(oracle.e4m3_encode([v])[0]) & 1) == 0]
+            assert gi == even[0], (xi, gi, near)
+        else:
+            assert abs(gi) == abs(near[0]), (xi, gi, near)
+
+
+def test_e4m3_round_agrees_with_torch_float8():
+    # torch's own float8_e4m3fn conversion (round to nearest even) as a second opinion
+    rng = np.random.default_rng(6)
+    x = np.concatenate([rng.uniform(-448, 448, 20000), rng.normal(0, 1, 20000)]).astype(np.float32)
+    x = x[np.abs(x) <= 448]
+    t = torch.from_numpy(x).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(oracle.e4m3_round(x.astype(np.float64)), t)
+
+
+def test_e4m3_encode_inverts_decode():
+    for c in range(256):
+        v = oracle.e4m3_decode(c)
+        if math.isnan(v) or c == 0x80:
+            continue
+        assert int(oracle.e4m3_encode([v])[0]) == c
+
+
+def test_fp8_block_exponent():
+    assert [oracle.fp8_block_exponent(a) for a in (448.0, 449.0, 1.0, 1.75, 1.76, 0.0)] == \
+        [0, 1, -8, -8, -7, 0]
+    rng = np.random.default_rng(7)
+    for a in np.exp(rng.uniform(-30, 30, 2000)):
+        e = oracle.fp8_block_exponent(a)
+        assert a / 2.0 ** e <= 448.0 < a / 2.0 ** (e - 1)      # the smallest such e
+
+
+def test_quantize_blocks_are_independent_and_exact_on_the_grid():
+    # block 0 holds e4m3 values (exponent 0 when its amax is 448), block 1 the
+    # same values times 2^-5: both quantise to themselves, and the scales differ
+    rng = np.random.default_rng(8)
+    grid = np.array([oracle.e4m3_decode(c) for c in range(0x00, 0x7F)])
+    a = rng.choice(grid, size=(64, 2, 16))
+    a[0, 0, 0] = 448.0
+    a[0, 1, 0] = 448.0
+    x = np.concatenate([a, a * 2.0 ** -5], axis=0)[None]           # [1, 128, 2, 16]
+    codes, exps, deq = oracle.quantize_qk_ref(x)
+    assert exps[0, :, 0].tolist() == [0, 0] and exps[0, :, 1].tolist() == [-5, -5]
+    assert np.array_equal(deq, x)
+    table = np.array([oracle.e4m3_decode(c) for c in range(256)])
+    scale = np.repeat(2.0 ** exps[0].T, 64, axis=0)[None, :, :, None]   # [1, 128, 2, 1]
+    assert np.array_equal(table[codes] * scale, x)
+
+
+def test_fp8_attention_reduces_to_exact_attention_on_the_grid():
+    # inputs already on each block's e4m3 grid: quantisation is the identity
+    rng = np.random.default_rng(9)
+    grid = np.array([oracle.e4m3_decode(c) for c in range(0x00, 0x7F)]) / 64.0
+    S, H, D = 150, 2, 16
+    q = rng.choice(grid, size=(1, S, H, D)) * rng.choice([-1, 1], size=(1, S, H, D))
+    k = rng.choice(grid, size=(1, S, H, D)) * rng.choice([-1, 1], size=(1, S, H, D))
+    v = rng.normal(size=(1, S, H, D))
+    for x in (q, k):     # pin every block's amax to 448 / 64 so its exponent is -6
+        for j in range(3):
+            x[0, 64 * j, :, 0] = 7.0
+    rp, ci = oracle.dense_csr(1, H, S)
+    o8, l8 = oracle.attn_fp8_ref(q, k, v, rp, ci)
+    o, l = oracle.attn_ref(q, k, v, rp, ci)
+    assert np.allclose(o8, o, rtol=0, atol=1e-12) and np.allclose(l8, l, rtol=0, atol=1e-12)
+
+
+def test_fp8_attention_sampled_items_equal_full():
+    cfg, q, k, v = sa_inputs.make_inputs("tiny")
+    ref = oracle.route_ref(q, k, cfg.P, float(np.float32(cfg.tau)))
+    rp, ci = ref["row_ptr"], ref["col_idx"]
+    o, l = oracle.attn_fp8_ref(q, k, v, rp, ci)
+    items = [(0, 1, 0), (0, 3, 7), (0, 3, 15)]
+    got = oracle.attn_fp8_ref(q, k, v, rp, ci, items=items)
+    for (b, h, i), (oi, li) in got.items():
+        assert np.array_equal(oi, o[b, 64 * i:64 * i + 64, h, :])
+        assert np.array_equal(li, l[b, h, 64 * i:64 * i + 64])
+    # and the 8-bit scores stay close to exact attention (a property, not a bound)
+    oe, _ = oracle.attn_ref(q, k, v, rp, ci)
+    assert np.linalg.norm(o - oe) / np.linalg.norm(oe) < 0.05

@@ -206,7 +206,8 @@ def run_ours(args):
     q, k, v = sa_inputs.make_qkv(cfg)
     B, S, H, D = q.shape
     qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
-    bufs = sa.alloc_layer_buffers(B, S, H, D, device=dev)
+    f8 = args.qk_format == "fp8"
+    bufs = sa.alloc_layer_buffers(B, S, H, D, device=dev, qk_format=args.qk_format)
     ws, status = bufs["ws"], bufs["status"]
     o, lse, rp_buf, ci_buf = bufs["o"], bufs["lse"], bufs["row_ptr"], bufs["col_idx"]
     stream = torch.cuda.current_stream(dev)
@@ -236,17 +237,19 @@ def run_ours(args):
         if ev is not None:
             ev[2].record(stream)
         if dense:
-            sa.sa_attn_dense(qa, ka, vd, o=o, lse=lse, workspace=ws, dev_status=status)
+            sa.sa_attn_dense(qa, ka, vd, o=o, lse=lse, workspace=ws, qk_format=args.qk_format,
+                             dev_status=status)
             if ev is not None:
                 ev[3].record(stream)
         else:
             # sa_attn_sparse as its two halves, so that the attention kernel
             # (the dominant one) is timed on its own
-            sa.sa_attn_prepare(vd, rp_buf, ci_buf, workspace=ws, q_block=qblk, dev_status=status)
+            sa.sa_attn_prepare(vd, rp_buf, ci_buf, workspace=ws, q_block=qblk,
+                               qk_format=args.qk_format, dev_status=status)
             if ev is not None:
                 ev[3].record(stream)
             sa.sa_attn_run(qa, ka, rp_buf, ci_buf, workspace=ws, v_like=vd, o=o, lse=lse,
-                           q_block=qblk, dev_status=status)
+                           q_block=qblk, qk_format=args.qk_format, dev_status=status)
         if ev is not None:
             ev[4].record(stream)
 
@@ -289,6 +292,10 @@ def run_ours(args):
     burst, sustained, _, peak_src = measured_peaks()
     long_region = total_ms > 1000.0
     peak = sustained if long_region else burst
+    if f8:
+        # half the FLOPs (Q.K^T) at the e4m3 rate, nominally twice bf16's, half
+        # (P.V) at the 16-bit rate: the mix's peak is 1 / (0.5/2 + 0.5) = 4/3 of bf16
+        peak = round(peak * 4.0 / 3.0, 1)
     achieved = flops / (kern_avg * 1e-3) / 1e12
     call_achieved = flops / (attn_avg * 1e-3) / 1e12
     sha = file_sha(os.path.join(ROOT, "block_sparse_attention_sa_gb300", "csrc", "attn.cu"))
@@ -297,12 +304,13 @@ def run_ours(args):
     traffic = (ATTN_TRAFFIC["bytes"]
                if ATTN_TRAFFIC["attn_cu_sha256"] and sha.startswith(ATTN_TRAFFIC["attn_cu_sha256"])
                and cfg.name == "release" and H == 56 and qblk == 64 and not dense and not pro
-               else None)
+               and not f8 else None)
 
-    e2e = None if (args.no_e2e or pro) else run_e2e(sa, cfg, q, k, v, bufs, flops, args, world, dev,
+    e2e = None if (args.no_e2e or pro or f8) else run_e2e(sa, cfg, q, k, v, bufs, flops, args, world, dev,
                                            stream, tau, mode, qblk)
     pairing = Nb > 2 and qblk == 64
-    per_step = ATTN_KERNELS + (0 if dense else ROUTE_KERNELS + (PAIR_KERNELS if pairing else 0))
+    per_step = (ATTN_KERNELS + (1 if f8 else 0)
+                + (0 if dense else ROUTE_KERNELS + (PAIR_KERNELS if pairing else 0)))
 
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
@@ -311,7 +319,7 @@ def run_ours(args):
         "data": "synthetic (seeded; stands in for the model's activations)",
         "config": {"workload": cfg.name, "B": B, "S": S, "H": H, "D": D, "prefix": cfg.P,
                    "tau": tau, "route_mode": "dense" if dense else mode, "block": 64,
-                   "q_block": qblk,
+                   "q_block": qblk, "qk_format": args.qk_format,
                    "density": round(density, 5),
                    "routed_tflop_per_layer": round(flops / 1e12, 4),
                    "ms_route": round(statistics.mean(route_ms), 4),
@@ -322,9 +330,7 @@ def run_ours(args):
                                              / 1e9, 1)} if pro else {}),
                    "ms_attn": round(attn_avg, 4),
                    "ms_attn_kernel": round(kern_avg, 4),
-                   "attn_call_frac": round(call_achieved / (
-                       measured_peaks()[1] if (ms_step * args.steps) > 1000.0
-                       else measured_peaks()[0]), 4),
+                   "attn_call_frac": round(call_achieved / peak, 4),
                    "l2": "inputs larger than L2 (Q/K/V/O %.2f GB), no flush" % (4 * q.numel() * 2 / 1e9),
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": {"bound": "tensor",
@@ -332,7 +338,9 @@ def run_ours(args):
                                 if dense else "attn_fwd_kernel"),
                      "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4),
-                     "peak_kind": f"{'sustained' if long_region else 'burst'} bf16, {peak_src}",
+                     "peak_kind": (f"{'sustained' if long_region else 'burst'} bf16, {peak_src}"
+                                   + (", x 4/3 for e4m3 Q.K^T + fp16 P.V (nominal e4m3 rate 2x bf16)"
+                                      if f8 else "")),
                      "traffic": traffic},
         "gpu_launches": per_step * args.steps,
         "e2e": e2e,
@@ -467,6 +475,8 @@ def main():
     ap.add_argument("--tau", type=float, default=None, help="override the workload's tau")
     ap.add_argument("--q-block", type=int, default=64, choices=[64, 128],
                     help="query block of the route (128: two key blocks per query block)")
+    ap.add_argument("--qk-format", default="bf16", choices=["bf16", "fp8"],
+                    help="arithmetic of the score product Q.K^T (fp8: 8-bit e4m3 scores)")
     ap.add_argument("--prologue", action="store_true",
                     help="QK-norm + RoPE in front, with the router's pooling fused in")
     ap.add_argument("--no-e2e", action="store_true")

@@ -12,6 +12,7 @@ Entry points (same names as the C ABI):
     sa_attn_sparse(q, k, v, row_ptr, col_idx, ...)    -> (o, lse)
     sa_attn_dense(q, k, v, ...)                       -> (o, lse)
     sa_qk_prologue(q, k, ...)                         -> (q_out, k_out, workspace)
+    sa_qk_quantize(q, k, ...)                         -> (q8, k8, q_exp, k_exp)
     sa_route_pooled(q_out, workspace, prefix_len, tau, ...) -> (row_ptr, col_idx)
     sa_forward_host(q_host, k_host, v_host, ...)      -> o_host (+ lse_host)
 Tensors are [B, S, H, D] bf16 with a contiguous last dimension.
@@ -30,6 +31,7 @@ __all__ = [
     "sa_qk_prologue", "sa_route_pooled", "sa_attn_prepare", "sa_attn_run",
     "sa_attn_sparse", "sa_attn_dense", "sa_forward_host", "sa_route_workspace_bytes",
     "sa_attn_workspace_bytes", "sa_route_max_nnz", "check_dev_status", "EXPORTS",
+    "sa_qk_quantize", "SA_QK_BF16", "SA_QK_FP8", "QK_FORMATS",
     "SA_DEV_CAPACITY", "SA_DEV_TIMEOUT", "SA_DEV_BAD_ROUTE", "SA_DEV_RANGE",
     "SA_ROUTE_THRESHOLD", "SA_ROUTE_DENSE_PREFIX_QUERIES", "SA_ROUTE_TOP_MASS", "ROUTE_MODES",
 ]
@@ -44,6 +46,9 @@ SA_ROUTE_THRESHOLD, SA_ROUTE_DENSE_PREFIX_QUERIES, SA_ROUTE_TOP_MASS = 0, 1, 2
 ROUTE_MODES = {"threshold": SA_ROUTE_THRESHOLD,
                "dense_prefix_queries": SA_ROUTE_DENSE_PREFIX_QUERIES,
                "top_mass": SA_ROUTE_TOP_MASS}
+# arithmetic of the score product (sa_params.qk_format)
+SA_QK_BF16, SA_QK_FP8 = 0, 1
+QK_FORMATS = {"bf16": SA_QK_BF16, "fp8": SA_QK_FP8}
 
 # Every function include/sa.h declares.
 EXPORTS = (
@@ -51,7 +56,7 @@ EXPORTS = (
     "sa_route_workspace_bytes", "sa_route", "sa_attn_workspace_bytes", "sa_attn_sparse",
     "sa_attn_dense", "sa_forward_host", "sa_dev_status_decode", "sa_status_string",
     "sa_route_static", "sa_qk_prologue", "sa_route_pooled", "sa_check_wait_timeout",
-    "sa_attn_prepare", "sa_attn_run",
+    "sa_attn_prepare", "sa_attn_run", "sa_qk_quantize",
 )
 SA_ROUTE_STATIC_WS_BYTES = 32 << 20
 
@@ -70,6 +75,7 @@ class sa_params(ctypes.Structure):
         ("q_stride", ctypes.c_int64 * 3), ("k_stride", ctypes.c_int64 * 3),
         ("v_stride", ctypes.c_int64 * 3), ("o_stride", ctypes.c_int64 * 3),
         ("route_mode", ctypes.c_int32), ("q_block", ctypes.c_int32),
+        ("qk_format", ctypes.c_int32),
     ]
 
 
@@ -110,6 +116,7 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         "sa_check_wait_timeout": (ctypes.c_int, [vp, vp]),
         "sa_attn_prepare": (ctypes.c_int, [P, vp, vp, vp, vp, sz, vp, vp]),
         "sa_attn_run": (ctypes.c_int, [P, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp]),
+        "sa_qk_quantize": (ctypes.c_int, [P, vp, vp, vp, vp, vp, vp, vp, vp]),
         "sa_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     }
     for name, (res, args) in sig.items():
@@ -157,10 +164,12 @@ def _require_cuda(*ts):
 
 def make_params(q: torch.Tensor, k: Optional[torch.Tensor] = None, v: Optional[torch.Tensor] = None,
                 o: Optional[torch.Tensor] = None, prefix_len: int = 0, tau: float = 1.0,
-                scale: float = 0.0, mode="threshold", q_block: int = 64) -> sa_params:
+                scale: float = 0.0, mode="threshold", q_block: int = 64,
+                qk_format="bf16") -> sa_params:
     B, S, H, D = q.shape
     p = sa_params()
     p.B, p.S, p.H, p.D, p.block, p.q_block = B, S, H, D, 64, int(q_block)
+    p.qk_format = QK_FORMATS[qk_format] if isinstance(qk_format, str) else int(qk_format)
     p.prefix_len, p.tau, p.softmax_scale = int(prefix_len), float(tau), float(scale)
     p.route_mode = ROUTE_MODES[mode] if isinstance(mode, str) else int(mode)
     for field, t in (("q_stride", q), ("k_stride", k if k is not None else q),
@@ -289,14 +298,15 @@ def sa_attn_sparse(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, row_ptr: t
                    col_idx: torch.Tensor, scale: float = 0.0, *, o: Optional[torch.Tensor] = None,
                    lse: Optional[torch.Tensor] = None, want_lse: bool = True,
                    workspace: Optional[torch.Tensor] = None, q_block: int = 64,
-                   dev_status: Optional[torch.Tensor] = None, stream=None):
+                   qk_format="bf16", dev_status: Optional[torch.Tensor] = None, stream=None):
     """Attention over the routed key blocks: (o bf16 [B,S,H,D], lse fp32 [B,H,S] or None).
     ``q_block`` = 128 when the route came from sa_route(..., q_block=128): the
-    kernel's tiles are then the 128-token query blocks, with no pairing step."""
+    kernel's tiles are then the 128-token query blocks, with no pairing step.
+    ``qk_format`` = "fp8" for 8-bit scores (see sa_qk_quantize)."""
     _require_cuda(q, k, v, row_ptr, col_idx)
     lib = load_library()
     o, lse = _attn_out(q, o, lse, want_lse)
-    p = make_params(q, k, v, o, scale=scale, q_block=q_block)
+    p = make_params(q, k, v, o, scale=scale, q_block=q_block, qk_format=qk_format)
     ws = _workspace(sa_attn_workspace_bytes(p), q.device, workspace)
     code = lib.sa_attn_sparse(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(row_ptr),
                               _ptr(col_idx), _ptr(o), _ptr(lse), _ptr(ws),
@@ -306,12 +316,12 @@ def sa_attn_sparse(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, row_ptr: t
 
 
 def sa_attn_prepare(v: torch.Tensor, row_ptr: torch.Tensor, col_idx: torch.Tensor, *,
-                    workspace: torch.Tensor, q_block: int = 64,
+                    workspace: torch.Tensor, q_block: int = 64, qk_format="bf16",
                     dev_status: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
     """First half of sa_attn_sparse: V repacked into ``workspace`` and the
     tile pairs chosen from the route. Returns the workspace."""
     _require_cuda(v, row_ptr, col_idx, workspace)
-    p = make_params(v, v, v, v, q_block=q_block)
+    p = make_params(v, v, v, v, q_block=q_block, qk_format=qk_format)
     if workspace.numel() * workspace.element_size() < sa_attn_workspace_bytes(p):
         raise ValueError("workspace too small")
     code = load_library().sa_attn_prepare(ctypes.byref(p), _ptr(v), _ptr(row_ptr), _ptr(col_idx),
@@ -325,13 +335,14 @@ def sa_attn_prepare(v: torch.Tensor, row_ptr: torch.Tensor, col_idx: torch.Tenso
 def sa_attn_run(q: torch.Tensor, k: torch.Tensor, row_ptr: torch.Tensor, col_idx: torch.Tensor,
                 scale: float = 0.0, *, workspace: torch.Tensor, v_like: Optional[torch.Tensor] = None,
                 o: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
-                want_lse: bool = True, q_block: int = 64,
+                want_lse: bool = True, q_block: int = 64, qk_format="bf16",
                 dev_status: Optional[torch.Tensor] = None, stream=None):
     """Second half of sa_attn_sparse: the attention kernel over a workspace
-    sa_attn_prepare filled. ``v_like`` gives V's strides (default q's)."""
+    sa_attn_prepare filled (with 8-bit scores, after quantising q and k into
+    it). ``v_like`` gives V's strides (default q's)."""
     _require_cuda(q, k, row_ptr, col_idx, workspace)
     o, lse = _attn_out(q, o, lse, want_lse)
-    p = make_params(q, k, v_like, o, scale=scale, q_block=q_block)
+    p = make_params(q, k, v_like, o, scale=scale, q_block=q_block, qk_format=qk_format)
     code = load_library().sa_attn_run(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(row_ptr),
                                       _ptr(col_idx), _ptr(o), _ptr(lse), _ptr(workspace),
                                       workspace.numel() * workspace.element_size(),
@@ -340,15 +351,33 @@ def sa_attn_run(q: torch.Tensor, k: torch.Tensor, row_ptr: torch.Tensor, col_idx
     return o, lse
 
 
+def sa_qk_quantize(q: torch.Tensor, k: torch.Tensor, *,
+                   dev_status: Optional[torch.Tensor] = None, stream=None):
+    """The e4m3 codes of q and k (uint8 [B,S,H,D]) and the scale exponents of
+    their 64-token blocks (int8 [B,H,Nb]); see sa.h."""
+    _require_cuda(q, k)
+    B, S, H, D = q.shape
+    nb = (S + 63) // 64
+    q8 = torch.empty((B, S, H, D), dtype=torch.uint8, device=q.device)
+    k8 = torch.empty_like(q8)
+    qe = torch.empty((B, H, nb), dtype=torch.int8, device=q.device)
+    ke = torch.empty_like(qe)
+    p = make_params(q, k)
+    code = load_library().sa_qk_quantize(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(q8), _ptr(k8),
+                                         _ptr(qe), _ptr(ke), _ptr(dev_status), _stream(stream))
+    _check(code, "sa_qk_quantize")
+    return q8, k8, qe, ke
+
+
 def sa_attn_dense(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float = 0.0, *,
                   o: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
                   want_lse: bool = True, workspace: Optional[torch.Tensor] = None,
-                  dev_status: Optional[torch.Tensor] = None, stream=None):
+                  qk_format="bf16", dev_status: Optional[torch.Tensor] = None, stream=None):
     """Attention over every key block (density 100%)."""
     _require_cuda(q, k, v)
     lib = load_library()
     o, lse = _attn_out(q, o, lse, want_lse)
-    p = make_params(q, k, v, o, scale=scale)
+    p = make_params(q, k, v, o, scale=scale, qk_format=qk_format)
     ws = _workspace(sa_attn_workspace_bytes(p), q.device, workspace)
     code = lib.sa_attn_dense(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
                              _ptr(ws), ws.numel() * ws.element_size(), _ptr(dev_status),
@@ -379,10 +408,10 @@ def sa_forward_host(q_host: torch.Tensor, k_host: torch.Tensor, v_host: torch.Te
     return o_host
 
 
-def alloc_layer_buffers(B: int, S: int, H: int, D: int, device="cuda") -> dict:
+def alloc_layer_buffers(B: int, S: int, H: int, D: int, device="cuda", qk_format="bf16") -> dict:
     """Device buffers for sa_forward_host (one workspace sized for both calls)."""
     q = torch.empty((B, S, H, D), dtype=torch.bfloat16, device=device)
-    p = make_params(q)
+    p = make_params(q, qk_format=qk_format)
     bufs = {"q": q, "k": torch.empty_like(q), "v": torch.empty_like(q), "o": torch.empty_like(q),
             "lse": torch.empty((B, H, S), dtype=torch.float32, device=device),
             "row_ptr": torch.empty(int(load_library().sa_route_rows(ctypes.byref(p))) + 1,

@@ -87,11 +87,12 @@ constexpr int kColO = 384;    // O at columns [384, 384 + D)
 // below fp16's normal range weigh under 2^-28 of the row max.
 constexpr float kRescaleLog2 = 14.0f;
 
-template <int D>
+template <int D, bool kF8>
 struct Smem {
-  static constexpr int kRegion = BM * 128;            // one 64-wide K slice of 128 rows
+  static constexpr int kRegion = BM * 128;            // one 128-byte-wide K slice of 128 rows
   static constexpr int kQ = 0;
-  static constexpr int kQBytes = BM * D * 2;
+  static constexpr int kQBytes = BM * D * (kF8 ? 1 : 2);  // bf16, or e4m3 codes
+  static constexpr int kQKSlices = kF8 ? D / 128 : D / 64;  // 128-byte slices of a Q/K row
   static constexpr int kStageBytes = BN * D * 2;      // one K tile or one V^T tile of a step
   static constexpr int kKV = kQ + kQBytes;
   static constexpr int kVHalf = D * 128;              // one 64-key half of a V^T tile
@@ -112,9 +113,11 @@ struct Smem {
   static constexpr int bFin = bOFree + 1;             // every MMA done (exit)
   static constexpr int kNumBars = bFin + 1;
   static constexpr int kMisc = kBar + kNumBars * 8;   // tmem base, abort flag
-  static constexpr int kHdr = kMisc + 16;             // [2][4] walk headers: b, h, pair, n
+  // [2][8] walk headers: b, h, pair, n, and (8-bit scores) the scale
+  // exponents of the tile's two query blocks
+  static constexpr int kHdr = kMisc + 16;
   // row exchange: [2 slots][2 warpgroups][BM] of (m, l, stop)
-  static constexpr int kXch = kHdr + 32;
+  static constexpr int kXch = kHdr + 64;
   static constexpr int kXchBytes = 2 * kSets * BM * 12;
   // running-max handoff: [2 warpgroups][BM] max after the warpgroup's latest
   // step, and that step's index in the CTA's sequence
@@ -122,7 +125,9 @@ struct Smem {
   static constexpr int kHandBytes = kSets * BM * 8;
   static constexpr int kBits = kHand + kHandBytes;
   static constexpr int kInfo = kBits + 2 * (kMaxNbAttn / 32) * 4;  // [2][kMaxNbAttn] walks
-  static constexpr int kEnd = kInfo + 2 * kMaxNbAttn * 2;
+  static constexpr int kKexp = kInfo + 2 * kMaxNbAttn * 2;  // [2][kMaxNbAttn] key-block
+                                                            // scale exponents of the walks
+  static constexpr int kEnd = kKexp + (kF8 ? 2 * kMaxNbAttn : 0);
   static constexpr int kBytes = kEnd + 1024;          // slack to align the base to 1 KB
 };
 
@@ -205,11 +210,11 @@ __device__ __forceinline__ void mask_tail32(uint32_t* v, uint32_t entry, int hal
   }
 }
 
-template <int D>
+template <int D, bool kF8>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_vt, const AttnArgs a) {
-  using L = Smem<D>;
+  using L = Smem<D, kF8>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -225,6 +230,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   const AbortSignal drain_sig{&never_flag, nullptr};  // drains wait out their own limit
   volatile int* hdr = reinterpret_cast<volatile int*>(smem + L::kHdr);
   uint16_t* info = reinterpret_cast<uint16_t*>(smem + L::kInfo);
+  int8_t* kexp = reinterpret_cast<int8_t*>(smem + L::kKexp);   // used with kF8 only
   auto bar = [&](int i) { return sbase + L::kBar + 8u * static_cast<uint32_t>(i); };
   auto fail = [&](int site) {
     *abort_flag = 1;
@@ -295,8 +301,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         if (lane == 0) fail(kSiteInfo);
         break;
       }
-      volatile int* hd = hdr + 4 * x;
+      volatile int* hd = hdr + 8 * x;
       uint16_t* inf = info + x * kMaxNbAttn;
+      int8_t* kx = kexp + x * kMaxNbAttn;
       if (tile >= a.n_tiles) {
         if (lane == 0) hd[3] = -1;   // no more tiles: every role leaves its loop
         __syncwarp();
@@ -328,8 +335,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       const int words = (Nb + 31) >> 5;
       if (a.row_ptr == nullptr) {
         const uint16_t m = has_qb1 ? 3 : 1;
-        for (int j = lane; j < Nb; j += 32)
+        for (int j = lane; j < Nb; j += 32) {
           inf[(j - qb0 + Nb) % Nb] = static_cast<uint16_t>((j << 2) | m);
+          if (kF8) kx[(j - qb0 + Nb) % Nb] = a.k_exp[static_cast<int64_t>(bh) * Nb + j];
+        }
         if (lane == 0) hd[3] = Nb;
       } else {
         for (int w = lane; w < words; w += 32) { bmA[w] = 0u; bmB[w] = 0u; }
@@ -388,6 +397,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             int rp = pos - below;
             if (rp < 0) rp += total;
             inf[rp] = static_cast<uint16_t>(((w * 32 + bit) << 2) | m);
+            if (kF8) kx[rp] = a.k_exp[static_cast<int64_t>(bh) * Nb + w * 32 + bit];
             ++pos;
             u &= u - 1;
           }
@@ -400,6 +410,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         hd[0] = b;
         hd[1] = h;
         hd[2] = static_cast<int>(static_cast<uint32_t>(qb0) | (static_cast<uint32_t>(qb1 & 0xffff) << 16));
+        if (kF8) {
+          hd[4] = a.q_exp[static_cast<int64_t>(bh) * Nb + qb0];
+          hd[5] = has_qb1 ? a.q_exp[static_cast<int64_t>(bh) * Nb + qb1] : 0;
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(L::bInfoFull + x));
@@ -418,7 +432,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       for (int it = 0;; ++it) {
         const int x = it & 1;
         if (!mbar_wait(bar(L::bInfoFull + x), (it >> 1) & 1, abort_sig)) { fail(kSiteInfo); break; }
-        const volatile int* hd = hdr + 4 * x;
+        const volatile int* hd = hdr + 8 * x;
         const int n = hd[3];
         if (n < 0) break;
         const int b = hd[0], h = hd[1];
@@ -433,7 +447,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         mbar_arrive_expect_tx(bar(L::bQFull), L::kQBytes);
         ++q_loads;
         for (int qh = 0; qh < 2; ++qh)
-          for (int dh = 0; dh < D / 64; ++dh)
+          for (int dh = 0; dh < L::kQKSlices; ++dh)
             tma_load_4d(sbase + L::kQ + dh * L::kRegion + qh * 8192, &tm_q, bar(L::bQFull),
                         dh * 64, qh ? qrow1 : qrow0, h, b);
         const int n_steps = (n + 1) >> 1;
@@ -445,13 +459,14 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             return false;
           }
           const int nblk = (2 * js + 1 < n) ? 2 : 1;
-          mbar_arrive_expect_tx(bar(L::bKVFull + st), nblk * kBlock * D * 2);
+          mbar_arrive_expect_tx(bar(L::bKVFull + st),
+                                nblk * kBlock * D * ((kF8 && kind == 0) ? 1 : 2));
           ++issued[st];
           const uint32_t dst = sbase + L::kKV + st * L::kStageBytes;
           for (int kh = 0; kh < nblk; ++kh) {
             const int jk = inf[2 * js + kh] >> 2;
             if (kind == 0) {
-              for (int dh = 0; dh < D / 64; ++dh)
+              for (int dh = 0; dh < L::kQKSlices; ++dh)
                 tma_load_4d(dst + dh * L::kRegion + kh * 8192, &tm_k, bar(L::bKVFull + st),
                             dh * 64, jk * kBlock, h, b);
             } else {
@@ -483,15 +498,17 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     // of the converged warp, so every commit tracks every earlier MMA). Order
     // per tile: QK(0), QK(1), then for each step j: QK(j+2) (if any), PV(j)
     // -- the same order in which the producer fills the ring.
-    constexpr uint32_t kIdQK128 = idesc_f16(BM, 128, 1);
-    constexpr uint32_t kIdQK64 = idesc_f16(BM, 64, 1);
+    constexpr uint32_t kIdQK128 = kF8 ? idesc_e4m3(BM, 128) : idesc_f16(BM, 128, 1);
+    constexpr uint32_t kIdQK64 = kF8 ? idesc_e4m3(BM, 64) : idesc_f16(BM, 64, 1);
+    // K slices of one MMA: 16 bf16 or 32 e4m3 values, 32 bytes either way
+    constexpr int kKS = kF8 ? D / 32 : D / 16;
     constexpr uint32_t kIdPV = idesc_f16(BM, D, 0);
     // Descriptors: Q's K slices (start address stepped by 32 bytes inside a
     // 128-byte swizzle row, then by one 16 KB region per 64 elements), and
     // the ring's base.
-    uint64_t qd[D / 16];
+    uint64_t qd[kKS];
 #pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk)
+    for (int kk = 0; kk < kKS; ++kk)
       qd[kk] = sdesc_kmajor_sw128(sbase + L::kQ + (kk >> 2) * L::kRegion + (kk & 3) * 32);
     const uint64_t kv0 = sdesc_kmajor_sw128(sbase + L::kKV);
     const uint32_t o_tmem = tmem + kColO;
@@ -504,7 +521,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         if (lane == 0) fail(kSiteInfo);
         break;
       }
-      const int n = hdr[4 * x + 3];
+      const int n = hdr[8 * x + 3];
       if (n < 0) break;
       const int n_steps = (n + 1) >> 1;
       if (!mbar_wait_warp(bar(L::bQFull), it & 1, abort_sig)) {
@@ -526,15 +543,21 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const uint32_t idesc = (2 * j + 1 < n) ? kIdQK128 : kIdQK64;
         const uint32_t d_tmem = tmem + kColS + b * 128;
         const uint64_t kb = kv0 + static_cast<uint64_t>(st * (L::kStageBytes >> 4));
-        uint64_t kd[D / 16];
+        uint64_t kd[kKS];
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
+        for (int kk = 0; kk < kKS; ++kk)
           kd[kk] = kb + static_cast<uint64_t>(((kk >> 2) * L::kRegion + (kk & 3) * 32) >> 4);
 #pragma unroll
-        for (int h4 = 0; h4 < D / 64; ++h4)
-          umma_ss_x4_elect(d_tmem, qd[4 * h4], qd[4 * h4 + 1], qd[4 * h4 + 2], qd[4 * h4 + 3],
-                           kd[4 * h4], kd[4 * h4 + 1], kd[4 * h4 + 2], kd[4 * h4 + 3], idesc,
-                           h4 > 0);
+        for (int h4 = 0; h4 < kKS / 4; ++h4) {
+          if (kF8)
+            umma_ss_x4_f8_elect(d_tmem, qd[4 * h4], qd[4 * h4 + 1], qd[4 * h4 + 2],
+                                qd[4 * h4 + 3], kd[4 * h4], kd[4 * h4 + 1], kd[4 * h4 + 2],
+                                kd[4 * h4 + 3], idesc, h4 > 0);
+          else
+            umma_ss_x4_elect(d_tmem, qd[4 * h4], qd[4 * h4 + 1], qd[4 * h4 + 2], qd[4 * h4 + 3],
+                             kd[4 * h4], kd[4 * h4 + 1], kd[4 * h4 + 2], kd[4 * h4 + 3], idesc,
+                             h4 > 0);
+        }
         umma_commit_elect(bar(L::bSFull + b));
         umma_commit_elect(bar(L::bKVEmpty + st));
         if (j == n_steps - 1) umma_commit_elect(bar(L::bQEmpty));  // Q no longer read
@@ -649,11 +672,13 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       if (stop && lane == 0) fail(kSiteInfo);
       float u0, u1;
       if (pair_xchg(0.f, 0.f, stop, u0, u1)) break;
-      const volatile int* hd = hdr + 4 * x;
+      const volatile int* hd = hdr + 8 * x;
       const int n = hd[3];
       if (n < 0) break;
       const int b = hd[0], h = hd[1];
       const uint32_t pr = static_cast<uint32_t>(hd[2]);
+      const int8_t* kx = kexp + x * kMaxNbAttn;
+      const int eq = kF8 ? hd[4 + qh] : 0;     // the row's query-block scale exponent
       const int qb = qh ? ((pr >> 16) == 0xffffu ? -1 : static_cast<int>(pr >> 16))
                         : static_cast<int>(pr & 0xffffu);
       const uint16_t* inf = info + x * kMaxNbAttn;
@@ -684,7 +709,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           tmem_ld32(lane_base + s_col + 64, sr + 64);
           tmem_ld32(lane_base + s_col + 96, sr + 96);
         }
-        float mx = -INFINITY;
+        // exp2-domain factor of each key block's logits: the softmax scale,
+        // times 2^(e_q + e_k) with 8-bit scores (exact: powers of two)
+        const float c0 = kF8 ? ldexpf(cl2, eq + kx[2 * j]) : cl2;
+        const float c1 = kF8 ? (two ? ldexpf(cl2, eq + kx[2 * j + 1]) : cl2) : cl2;
+        float mx0 = -INFINITY, mx1 = -INFINITY;
         if (mem0 || mem1) {
           tmem_wait_ld();
           if (mem0) {
@@ -692,17 +721,18 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             reg_fence32(sr + 32);
             mask_tail32(sr, e0, 0, Nb, last_valid);
             mask_tail32(sr + 32, e0, 1, Nb, last_valid);
-            mx = fmaxf(max32(sr), max32(sr + 32));
+            mx0 = fmaxf(max32(sr), max32(sr + 32));
           }
           if (mem1) {
             reg_fence32(sr + 64);
             reg_fence32(sr + 96);
             mask_tail32(sr + 64, e1, 0, Nb, last_valid);
             mask_tail32(sr + 96, e1, 1, Nb, last_valid);
-            mx = fmaxf(mx, fmaxf(max32(sr + 64), max32(sr + 96)));
+            mx1 = fmaxf(max32(sr + 64), max32(sr + 96));
           }
         }
-        const float bmax = mx * cl2;             // the scale is positive: max commutes
+        // the factors are positive: the max commutes with them
+        const float bmax = fmaxf(mx0 * c0, mx1 * c1);
         // the running max after step g - 1 (none before the tile's first step)
         float m_prev = -INFINITY;
         if (j > 0) {
@@ -749,8 +779,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         {
           uint32_t pk[32];
           if (mem0) {
-            rs = exp_pack32(sr, cl2, -m_new, pk);
-            rs += exp_pack32(sr + 32, cl2, -m_new, pk + 16);
+            rs = exp_pack32(sr, c0, -m_new, pk);
+            rs += exp_pack32(sr + 32, c0, -m_new, pk + 16);
           } else {
 #pragma unroll
             for (int u = 0; u < 32; ++u) pk[u] = 0u;
@@ -760,8 +790,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         if (two) {
           uint32_t pk[32];
           if (mem1) {
-            rs += exp_pack32(sr + 64, cl2, -m_new, pk);
-            rs += exp_pack32(sr + 96, cl2, -m_new, pk + 16);
+            rs += exp_pack32(sr + 64, c1, -m_new, pk);
+            rs += exp_pack32(sr + 96, c1, -m_new, pk + 16);
           } else {
 #pragma unroll
             for (int u = 0; u < 32; ++u) pk[u] = 0u;
@@ -883,18 +913,18 @@ pack_v_kernel(const uint16_t* __restrict__ v, int64_t vs0, int64_t vs1, int64_t 
   if (__syncthreads_or(range) && threadIdx.x == 0) set_status(dev_status, SA_DEV_RANGE);
 }
 
-template <int D>
+template <int D, bool kF8>
 cudaError_t launch_attn_d(const AttnMaps& m, const AttnArgs& a, cudaStream_t st) {
-  constexpr int smem = Smem<D>::kBytes;
+  constexpr int smem = Smem<D, kF8>::kBytes;
   static_assert(smem <= 227 * 1024, "attention tile does not fit shared memory");
-  cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D>,
+  cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D, kF8>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int grid = a.n_tiles < sms ? a.n_tiles : sms;   // persistent: one CTA per SM
-  attn_fwd_kernel<D><<<grid, kThreads, smem, st>>>(m.q, m.k, m.vt, a);
+  attn_fwd_kernel<D, kF8><<<grid, kThreads, smem, st>>>(m.q, m.k, m.vt, a);
   return cudaGetLastError();
 }
 
@@ -912,7 +942,8 @@ cudaError_t launch_pack_v(const uint16_t* v, const int64_t vs[3], int B, int S, 
 }
 
 cudaError_t launch_attn(int D, const AttnMaps& m, const AttnArgs& a, cudaStream_t st) {
-  return D == 128 ? launch_attn_d<128>(m, a, st) : launch_attn_d<64>(m, a, st);
+  if (a.q_exp != nullptr) return launch_attn_d<128, true>(m, a, st);   // 8-bit scores: D = 128
+  return D == 128 ? launch_attn_d<128, false>(m, a, st) : launch_attn_d<64, false>(m, a, st);
 }
 
 }  // namespace sa

@@ -364,6 +364,35 @@ __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, int ab_type) {
          | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
 }
 
+// Instruction descriptor, kind::f8f6f4 with fp32 accumulation, both operands
+// e4m3 (format code 0) and K-major.
+__host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N) {
+  return (1u << 4)                                   // D format: fp32
+         | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
+         | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
+}
+
+// Four kind::f8f6f4 MMAs (K = 32 each) back to back into one accumulator,
+// issued by the lane elect.sync picks; the first overwrites D unless
+// `accumulate` is set.
+__device__ __forceinline__ void umma_ss_x4_f8_elect(uint32_t d_tmem, uint64_t a0, uint64_t a1,
+                                                    uint64_t a2, uint64_t a3, uint64_t b0,
+                                                    uint64_t b1, uint64_t b2, uint64_t b3,
+                                                    uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p, t;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %10, 0;\n\t"
+      "setp.eq.b32 t, %10, %10;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %5, %9, p;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %2, %6, %9, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %3, %7, %9, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %4, %8, %9, t;\n\t}"
+      ::"r"(d_tmem), "l"(a0), "l"(a1), "l"(a2), "l"(a3), "l"(b0), "l"(b1), "l"(b2), "l"(b3),
+        "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // 32 lanes x 32 consecutive 32-bit columns: thread t of the warp gets lane
 // (base lane + t), columns [col, col + 32).
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {

@@ -47,7 +47,9 @@ sa_status check_params(const sa_params* p) {
     return SA_ERR_INVALID_ARG;
   if (p->q_block != 0 && p->q_block != kBlock && p->q_block != 2 * kBlock) return SA_ERR_INVALID_ARG;
   if (p->route_mode == SA_ROUTE_TOP_MASS && p->tau > 1.f) return SA_ERR_INVALID_ARG;
+  if (p->qk_format != SA_QK_BF16 && p->qk_format != SA_QK_FP8) return SA_ERR_INVALID_ARG;
   if (p->D != 64 && p->D != 128) return p->D > 0 ? SA_ERR_UNSUPPORTED : SA_ERR_INVALID_ARG;
+  if (p->qk_format == SA_QK_FP8 && p->D != 128) return SA_ERR_UNSUPPORTED;
   if (p->H > 65535 || p->B > 65535) return SA_ERR_UNSUPPORTED;
   const int64_t nb = num_blocks(p->S);
   const int64_t max_nnz = static_cast<int64_t>(p->B) * p->H * nb * nb;
@@ -103,13 +105,37 @@ size_t vt_bytes(const sa_params* p) {
   return static_cast<size_t>(p->B) * p->H * p->D * s_pad_of(p->S) * 2;
 }
 
+// e4m3 codes [B, S, H, D], contiguous -> 4-D map (D, S, H, B), box 128 x 64
+// (one 128-byte row per token), 128-byte swizzle.
+sa_status encode_bshd_u8(CUtensorMap* m, const void* base, const sa_params* p) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return SA_ERR_CUDA;
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(p->D), static_cast<cuuint64_t>(p->S),
+                              static_cast<cuuint64_t>(p->H), static_cast<cuuint64_t>(p->B)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(p->H) * p->D,
+                                 static_cast<cuuint64_t>(p->D),
+                                 static_cast<cuuint64_t>(p->S) * p->H * p->D};
+  const cuuint32_t box[4] = {128, 64, 1, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? SA_OK : SA_ERR_INVALID_ARG;
+}
+
+size_t codes_bytes(const sa_params* p) {
+  return static_cast<size_t>(p->B) * p->S * p->H * p->D;
+}
+
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 // Attention workspace, each part 256-byte aligned: V repacked to fp16, the
-// persistent kernel's tile counter, the pairing's candidate lists and its
+// persistent kernel's tile counter, the pairing's candidate lists, with
+// 8-bit scores the e4m3 codes of Q and K and their scale exponents, and the
 // tile list (last).
 struct AttnLayout {
-  size_t vt, counter, cand, pairs, total;
+  size_t vt, counter, cand, q8, k8, qexp, kexp, pairs, total;
 };
 
 AttnLayout attn_layout(const sa_params* p) {
@@ -119,7 +145,12 @@ AttnLayout attn_layout(const sa_params* p) {
   L.vt = 0;
   L.counter = align256(vt_bytes(p));
   L.cand = L.counter + 256;
-  L.pairs = L.cand + align256(pair_cand_bytes(bh * Nb));
+  L.q8 = L.cand + align256(pair_cand_bytes(bh * Nb));
+  const bool f8 = p->qk_format == SA_QK_FP8;
+  L.k8 = L.q8 + (f8 ? align256(codes_bytes(p)) : 0);
+  L.qexp = L.k8 + (f8 ? align256(codes_bytes(p)) : 0);
+  L.kexp = L.qexp + (f8 ? align256(static_cast<size_t>(bh) * Nb) : 0);
+  L.pairs = L.kexp + (f8 ? align256(static_cast<size_t>(bh) * Nb) : 0);
   L.total = L.pairs + align256(static_cast<size_t>(bh) * ((Nb + 1) / 2) * sizeof(uint32_t));
   return L;
 }
@@ -185,12 +216,39 @@ sa_status attn_run_launch(const sa_params* p, const void* q, const void* k,
   sa_status s;
   AttnMaps maps;
   std::memset(&maps, 0, sizeof(maps));
-  if ((s = encode_bshd(&maps.q, q, p, p->q_stride)) != SA_OK) return s;
-  if ((s = encode_bshd(&maps.k, k, p, p->k_stride)) != SA_OK) return s;
-  if ((s = encode_vt(&maps.vt, ws, p)) != SA_OK) return s;
   const AttnLayout L = attn_layout(p);
   char* wsb = static_cast<char*>(ws);
   const int Nb = num_blocks(p->S);
+  const bool f8 = p->qk_format == SA_QK_FP8;
+  if (f8) {
+    // 8-bit scores: Q and K quantised into the workspace first
+    QuantArgs qa{};
+    qa.q = static_cast<const uint16_t*>(q);
+    qa.k = static_cast<const uint16_t*>(k);
+    for (int i = 0; i < 3; ++i) {
+      qa.qs[i] = p->q_stride[i];
+      qa.ks[i] = p->k_stride[i];
+    }
+    qa.q8 = reinterpret_cast<uint8_t*>(wsb + L.q8);
+    qa.k8 = reinterpret_cast<uint8_t*>(wsb + L.k8);
+    qa.y_stride[0] = static_cast<int64_t>(p->S) * p->H * p->D;
+    qa.y_stride[1] = static_cast<int64_t>(p->H) * p->D;
+    qa.y_stride[2] = p->D;
+    qa.q_exp = reinterpret_cast<int8_t*>(wsb + L.qexp);
+    qa.k_exp = reinterpret_cast<int8_t*>(wsb + L.kexp);
+    qa.B = p->B;
+    qa.S = p->S;
+    qa.H = p->H;
+    qa.Nb = Nb;
+    qa.dev_status = dev_status;
+    if (launch_quant(qa, st) != cudaSuccess) return SA_ERR_CUDA;
+    if ((s = encode_bshd_u8(&maps.q, wsb + L.q8, p)) != SA_OK) return s;
+    if ((s = encode_bshd_u8(&maps.k, wsb + L.k8, p)) != SA_OK) return s;
+  } else {
+    if ((s = encode_bshd(&maps.q, q, p, p->q_stride)) != SA_OK) return s;
+    if ((s = encode_bshd(&maps.k, k, p, p->k_stride)) != SA_OK) return s;
+  }
+  if ((s = encode_vt(&maps.vt, ws, p)) != SA_OK) return s;
   AttnArgs a{};
   a.row_ptr = dense ? nullptr : row_ptr;
   a.col_idx = dense ? nullptr : col_idx;
@@ -210,6 +268,8 @@ sa_status attn_run_launch(const sa_params* p, const void* q, const void* k,
   // the tile counter and the launch's abort word, zeroed together
   a.tile_counter = reinterpret_cast<int*>(wsb + L.counter);
   a.grid_abort = a.tile_counter + 1;
+  a.q_exp = f8 ? reinterpret_cast<const int8_t*>(wsb + L.qexp) : nullptr;
+  a.k_exp = f8 ? reinterpret_cast<const int8_t*>(wsb + L.kexp) : nullptr;
   if (cudaMemsetAsync(a.tile_counter, 0, 2 * sizeof(int), st) != cudaSuccess) return SA_ERR_CUDA;
   return from_cuda(launch_attn(p->D, maps, a, st));
 }
@@ -426,6 +486,39 @@ sa_status sa_route_pooled(const sa_params* p, int32_t* row_ptr, int32_t* col_idx
                  &a);
   if (s != SA_OK) return s;
   return from_cuda(launch_route_select(a, static_cast<cudaStream_t>(stream)));
+}
+
+sa_status sa_qk_quantize(const sa_params* p, const void* q, const void* k, uint8_t* q8,
+                         uint8_t* k8, int8_t* q_exp, int8_t* k_exp, int32_t* dev_status,
+                         void* stream) {
+  sa_status s = check_params(p);
+  if (s != SA_OK) return s;
+  if (p->D != 128) return SA_ERR_UNSUPPORTED;
+  if (!q || !k || !q8 || !k8 || !q_exp || !k_exp) return SA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || (reinterpret_cast<uintptr_t>(q8) & 7u) != 0 ||
+      (reinterpret_cast<uintptr_t>(k8) & 7u) != 0)
+    return SA_ERR_INVALID_ARG;
+  if (!strides_ok(p->q_stride) || !strides_ok(p->k_stride)) return SA_ERR_INVALID_ARG;
+  QuantArgs qa{};
+  qa.q = static_cast<const uint16_t*>(q);
+  qa.k = static_cast<const uint16_t*>(k);
+  for (int i = 0; i < 3; ++i) {
+    qa.qs[i] = p->q_stride[i];
+    qa.ks[i] = p->k_stride[i];
+  }
+  qa.q8 = q8;
+  qa.k8 = k8;
+  qa.y_stride[0] = static_cast<int64_t>(p->S) * p->H * p->D;
+  qa.y_stride[1] = static_cast<int64_t>(p->H) * p->D;
+  qa.y_stride[2] = p->D;
+  qa.q_exp = q_exp;
+  qa.k_exp = k_exp;
+  qa.B = p->B;
+  qa.S = p->S;
+  qa.H = p->H;
+  qa.Nb = num_blocks(p->S);
+  qa.dev_status = dev_status;
+  return from_cuda(launch_quant(qa, static_cast<cudaStream_t>(stream)));
 }
 
 sa_status sa_attn_sparse(const sa_params* p, const void* q, const void* k, const void* v,

@@ -104,11 +104,30 @@ struct AttnArgs {
   int* grid_abort;         // zeroed before the launch; set by a CTA whose wait gave up
   int64_t nnz_row;         // B*H*Nb: row_ptr[nnz_row] is the route's entry count
   int n_tiles;             // B * H * n_pairs
+  const int8_t* q_exp;     // 8-bit scores: [B*H*Nb] scale exponents (nullptr: bf16)
+  const int8_t* k_exp;
 };
 
 struct AttnMaps {
-  CUtensorMap q, k, vt;
+  CUtensorMap q, k, vt;    // q, k: bf16, or the e4m3 codes for 8-bit scores
 };
+
+// 8-bit (e4m3) copies of Q and K with one power-of-two scale exponent per
+// (batch, head, 64-token block); D = 128.
+struct QuantArgs {
+  const uint16_t* q;       // bf16 bits
+  const uint16_t* k;
+  int64_t qs[3], ks[3];    // element strides of b, s, h
+  uint8_t* q8;             // e4m3 codes, [B, S, H, D] with strides y_stride (bytes)
+  uint8_t* k8;
+  int64_t y_stride[3];
+  int8_t* q_exp;           // [B*H*Nb] scale exponents
+  int8_t* k_exp;
+  int B, S, H, Nb;
+  int32_t* dev_status;
+};
+
+cudaError_t launch_quant(const QuantArgs& a, cudaStream_t st);
 
 // Repacks V [B,S,H,D] bf16 into vt [B*H][D][s_pad] fp16 (key-contiguous).
 cudaError_t launch_pack_v(const uint16_t* v, const int64_t vs[3], int B, int S, int H, int D,

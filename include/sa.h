@@ -62,6 +62,14 @@ enum {
                                P.V product runs in fp16, see sa_attn_sparse    */
 };
 
+/* Arithmetic of the attention's score product Q.K^T (sa_attn_*). */
+enum {
+  SA_QK_BF16 = 0,   /* bf16 x bf16 -> fp32 (the default)                       */
+  SA_QK_FP8 = 1     /* 8-bit scores: Q and K quantised to e4m3 per (batch,
+                       head, 64-token block) with power-of-two scales, see
+                       sa_qk_quantize; D = 128 only                           */
+};
+
 /* Readings of the router rule (sa_route; the pages leave the rule open). */
 enum {
   SA_ROUTE_THRESHOLD = 0,           /* keep p_ij >= tau / Nb (the default)     */
@@ -88,10 +96,12 @@ typedef struct sa_params {
   int32_t route_mode;     /* SA_ROUTE_*; sa_params_init sets THRESHOLD       */
   int32_t q_block;        /* query block of the route: 0 or 64 (square, the
                              default) or 128 (two key blocks); see sa_route  */
+  int32_t qk_format;      /* SA_QK_*; sa_params_init sets SA_QK_BF16         */
 } sa_params;
 
 /* Fills p for a contiguous [B, S, H, D] layout of all four tensors, with
- * route_mode = SA_ROUTE_THRESHOLD, q_block = 0 and softmax_scale = 0. */
+ * route_mode = SA_ROUTE_THRESHOLD, q_block = 0, qk_format = SA_QK_BF16 and
+ * softmax_scale = 0. */
 void sa_params_init(sa_params* p, int32_t B, int32_t S, int32_t H, int32_t D,
                     int32_t prefix_len, float tau);
 
@@ -238,7 +248,32 @@ sa_status sa_route_pooled(const sa_params* p, int32_t* row_ptr, int32_t* col_idx
                           int64_t col_cap, void* workspace, size_t ws_bytes,
                           int32_t* dev_status, void* stream);
 
-/* Bytes of device workspace sa_attn_sparse / sa_attn_dense need. */
+/*
+ * sa_qk_quantize -- the 8-bit copies of q and k that sa_attn_* use with
+ * p->qk_format = SA_QK_FP8 (MiniAcc blog, "What is SageAttention?": the
+ * score computation in 8-bit arithmetic; the format and scaling are this
+ * library's reading: FP8 e4m3, the 8-bit format GB300's tensor cores run
+ * fastest). For every (b, h, 64-token block j) of q, and of k:
+ *   e     = the smallest integer with amax / 2^e <= 448, where amax is the
+ *           largest |x| over the block's valid tokens and all D (e = 0 for
+ *           an all-zero block);
+ *   code  = x / 2^e rounded to the nearest e4m3 value, ties to even
+ *           (exact scaling: the scale is a power of two).
+ * The attention's logits are then scale * 2^(e_q + e_k) * (codes_q . codes_k).
+ *
+ * q, k          device bf16 [B, S, H, D] (strides in p), D = 128.
+ * q8, k8        device uint8 [B, S, H, D], contiguous, 8-byte aligned: the
+ *               e4m3 codes (tokens >= S are not written).
+ * q_exp, k_exp  device int8 [B*H*Nb]: e of block (b, h, j) at (b*H + h)*Nb + j.
+ * A non-finite input raises SA_DEV_RANGE (its block's codes are undefined).
+ * Errors: SA_ERR_INVALID_ARG / SA_ERR_UNSUPPORTED (D != 128) before launch.
+ */
+sa_status sa_qk_quantize(const sa_params* p, const void* q, const void* k, uint8_t* q8,
+                         uint8_t* k8, int8_t* q_exp, int8_t* k_exp, int32_t* dev_status,
+                         void* stream);
+
+/* Bytes of device workspace sa_attn_sparse / sa_attn_dense need (more with
+ * p->qk_format = SA_QK_FP8: the codes of Q and K live there). */
 size_t sa_attn_workspace_bytes(const sa_params* p);
 
 /*
@@ -253,10 +288,13 @@ size_t sa_attn_workspace_bytes(const sa_params* p);
  * Only the listed K/V blocks are read. A row with an empty list gives o = 0
  * and lse = -inf.
  *
- * Precision: Q.K^T is a bf16 x bf16 product with fp32 accumulation; the
- * softmax is fp32; the P.V product takes P and V in fp16 (V is repacked once
- * per call into the workspace) with fp32 accumulation; o is rounded once to
- * bf16. |v| must be <= 65504 (else SA_DEV_RANGE).
+ * Precision: Q.K^T is a bf16 x bf16 product with fp32 accumulation (with
+ * p->qk_format = SA_QK_FP8: an e4m3 x e4m3 product of sa_qk_quantize's codes,
+ * fp32 accumulation, times the blocks' power-of-two scales; the codes are
+ * made in the workspace by each call); the softmax is fp32; the P.V product
+ * takes P and V in fp16 (V is repacked once per call into the workspace)
+ * with fp32 accumulation; o is rounded once to bf16. |v| must be <= 65504
+ * (else SA_DEV_RANGE).
  *
  * q, k, v    device bf16 [B, S, H, D] (strides in p); not modified.
  * row_ptr,   device int32 CSR as written by sa_route: row_ptr[B*H*Nb] = nnz
@@ -290,7 +328,8 @@ sa_status sa_attn_sparse(const sa_params* p, const void* q, const void* k,
  * sa_attn_prepare, sa_attn_run -- sa_attn_sparse in two calls, with the same
  * result: sa_attn_prepare repacks V into the workspace and (for 64-token
  * query blocks) chooses the tile pairs from the route; sa_attn_run launches
- * the attention kernel over that workspace. Between them the caller may
+ * the attention kernel over that workspace (with SA_QK_FP8, after quantising
+ * q and k into it, as sa_qk_quantize does). Between them the caller may
  * enqueue other work (or time the kernel alone); sa_attn_run must see the
  * same p, route and workspace, after sa_attn_prepare on the same stream (or
  * ordered after it), and V unchanged. Arguments and errors as

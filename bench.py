@@ -315,7 +315,10 @@ def run_ours(args):
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        # the arithmetic of the path: Q.K^T operands, P.V operands, accumulation
+        "dtype": ("e4m3 QK, fp16 PV, fp32 accumulate" if f8
+                  else "bf16 QK, fp16 PV, fp32 accumulate"),
         "data": "synthetic (seeded; stands in for the model's activations)",
         "config": {"workload": cfg.name, "B": B, "S": S, "H": H, "D": D, "prefix": cfg.P,
                    "tau": tau, "route_mode": "dense" if dense else mode, "block": 64,
@@ -347,8 +350,11 @@ def run_ours(args):
         "clocks": clk.summary(),
     }
     if world == 1 and not args.no_cpu and rank == 0:
+        # the oracle times the whole layer where it finishes in about a minute
+        # (tiny, mid), else a bounded sample scaled to the layer
         result["cpu_baseline"] = cpu_baseline(cfg, q, k, v, flops, budget_s=15.0, tau=tau,
-                                              mode=mode, q_block=qblk)
+                                              mode=mode, q_block=qblk,
+                                              full_layer=cfg.name in ("tiny", "mid") and not f8)
     if rank == 0:
         print(json.dumps(result), flush=True)
     if world > 1:
@@ -392,9 +398,26 @@ def run_e2e(sa, cfg, q, k, v, bufs, flops, args, world, dev, stream, tau, mode, 
 
 # ------------------------------------------------------- the CPU oracle ----
 
+def blas_threads():
+    """(threads, how) of the BLAS numpy calls: threadpoolctl's report where it
+    is installed, else the thread-count variables, else None."""
+    try:
+        from threadpoolctl import threadpool_info
+        n = [d["num_threads"] for d in threadpool_info() if d.get("user_api") == "blas"]
+        if n:
+            return int(max(n)), "threadpoolctl"
+    except Exception:
+        pass
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(var, "").isdigit():
+            return int(os.environ[var]), var
+    return None, "not reported by the BLAS (its default is one thread per core)"
+
+
 def cpu_baseline(cfg, q, k, v, flops, budget_s=15.0, seed=0, tau=None, mode="threshold",
-                 q_block=64):
-    """Time the oracle on a bounded sample of the layer and scale to a whole
+                 q_block=64, full_layer=False):
+    """Time the oracle on the layer. With ``full_layer`` the whole layer (every
+    head routed and attended); otherwise a bounded sample scaled to a whole
     layer: the route of one head in full, plus as many query blocks of that
     head as fit in ``budget_s`` (at least 4), extrapolated linearly to all
     heads and blocks."""
@@ -402,11 +425,23 @@ def cpu_baseline(cfg, q, k, v, flops, budget_s=15.0, seed=0, tau=None, mode="thr
 
     B, S, H, D = q.shape
     Nb = cfg.Nb
-    h = seed % H
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    threads, how = blas_threads()
+    tau = cfg.tau if tau is None else tau
+    if full_layer:
+        t0 = time.perf_counter()
+        r = oracle.route_ref(q, k, cfg.P, float(np.float32(tau)), mode=mode, q_block=q_block)
+        t_route = time.perf_counter() - t0
+        oracle.attn_ref(q, k, v, r["row_ptr"], r["col_idx"])
+        layer_s = time.perf_counter() - t0
+        return {"value": round(flops / layer_s / 1e12, 6), "unit": UNIT, "cores": cores,
+                "threads": threads, "threads_source": how, "kind": "oracle",
+                "timing": "the full layer, timed once",
+                "sample": f"the full layer: {B * H} heads routed ({t_route:.1f} s) and "
+                          f"attended, {layer_s:.1f} s"}
+    h = seed % H
     qs, ks, vs = (t[:, :, h:h + 1].contiguous() for t in (q, k, v))
     t0 = time.perf_counter()
-    tau = cfg.tau if tau is None else tau
     r = oracle.route_ref(qs, ks, cfg.P, float(np.float32(tau)), mode=mode, q_block=q_block)
     t_route = time.perf_counter() - t0
     order = np.random.default_rng(seed).permutation(Nb)
@@ -419,7 +454,9 @@ def cpu_baseline(cfg, q, k, v, flops, budget_s=15.0, seed=0, tau=None, mode="thr
         n_done += 1
     layer_s = t_route * B * H + t_attn * (B * H * Nb / n_done)
     return {"value": round(flops / layer_s / 1e12, 6), "unit": UNIT, "cores": cores,
-            "kind": "oracle",
+            "threads": threads, "threads_source": how, "kind": "oracle",
+            "timing": "extrapolated from a sample",
+            "sampled_s": round(t_route + t_attn, 2),
             "sample": f"head {h}: full route ({t_route:.1f} s) + {n_done} query blocks of "
                       f"attention ({t_attn:.1f} s); extrapolated linearly to {B * H} heads x "
                       f"{Nb} blocks = {layer_s:.0f} s per layer"}
@@ -446,15 +483,22 @@ def run_reference(args):
                          q_block=qblk) for s in range(args.steps)]
     value = statistics.mean(c["value"] for c in vals)
     ms = flops / (value * 1e12) * 1e3
+    sampled = statistics.mean(c["sampled_s"] for c in vals)
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT,
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(ms, 1), "higher_is_better": True, "scaling": "weak",
+        "timing": (f"extrapolated from a sample: each of the {args.steps} steps times "
+                   f"{sampled:.1f} s of the oracle (one head routed in full and a sample of its "
+                   f"query blocks attended) and scales it linearly to the whole layer; "
+                   f"ms_per_step is that extrapolated layer time, not a step's wall time"),
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
         "config": {"workload": cfg.name, "B": B, "S": S, "H": H, "D": D, "prefix": cfg.P,
                    "tau": tau, "route_mode": mode, "q_block": qblk},
         "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": vals[0]["cores"],
-                         "kind": "oracle", "sample": vals[-1]["sample"]},
+                         "threads": vals[0]["threads"],
+                         "threads_source": vals[0]["threads_source"], "kind": "oracle",
+                         "timing": "extrapolated from a sample", "sample": vals[-1]["sample"]},
         "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }), flush=True)

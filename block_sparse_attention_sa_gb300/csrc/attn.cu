@@ -129,6 +129,10 @@ struct Smem {
                                                             // scale exponents of the walks
   static constexpr int kEnd = kKexp + (kF8 ? 2 * kMaxNbAttn : 0);
   static constexpr int kBytes = kEnd + 1024;          // slack to align the base to 1 KB
+  static_assert(kBar % 8 == 0 && kMisc % 8 == 0 && kHdr % 4 == 0 && kXch % 4 == 0,
+                "barrier, header and exchange alignment");
+  static_assert(kHand % 8 == 0 && kBits % 4 == 0 && kInfo % 2 == 0,
+                "shared-memory region alignment");
 };
 
 __device__ __forceinline__ uint32_t pack_half2(float a, float b) {
@@ -564,19 +568,33 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         ++c;
         return true;
       };
-      if (n_steps == 0) umma_commit_elect(bar(L::bQEmpty));
+      // The previous tile's epilogue must have read O before this tile's
+      // first PV overwrites it. The wait sits right before that PV, so the
+      // epilogue overlaps this tile's first three Q.K^T products (an empty
+      // tile waits before its tile_done, so that barrier never runs a phase
+      // ahead of the epilogue that waits on it).
+      auto wait_o_free = [&]() -> bool {
+        if (it >= 1 && !mbar_wait_warp(bar(L::bOFree), (it - 1) & 1, abort_sig)) {
+          if (lane == 0) fail(kSiteOFree);
+          return false;
+        }
+        tc_fence_after();
+        return true;
+      };
+      if (n_steps == 0) {
+        umma_commit_elect(bar(L::bQEmpty));
+        ok = wait_o_free();
+      }
       for (int j = 0; j < 2 && j < n_steps && ok; ++j) ok = issue_qk(j);
       if (!ok) break;
-      // the previous tile's epilogue has read O
-      if (it >= 1 && !mbar_wait_warp(bar(L::bOFree), (it - 1) & 1, abort_sig)) {
-        if (lane == 0) fail(kSiteOFree);
-        break;
-      }
-      tc_fence_after();
       for (int j = 0; j < n_steps && ok; ++j) {
         // QK(j+2) needs no softmax result, so it goes first: the tensor pipe
         // works on it while this warp waits for P(j).
         if (j + 2 < n_steps && !issue_qk(j + 2)) {
+          ok = false;
+          break;
+        }
+        if (j == 0 && !wait_o_free()) {
           ok = false;
           break;
         }

@@ -152,3 +152,48 @@ def test_fp8_needs_head_dim_128(sa):
     q, k, v = sa_inputs.random_small(128, 1, 64, seed=3)
     with pytest.raises(sa.SaError):
         sa.sa_attn_dense(q.cuda(), k.cuda(), v.cuda(), qk_format="fp8")
+
+
+def test_fp8_batch_and_strided_views(sa):
+    # B = 2, heads 1..3 of a 5-head buffer: the quantiser reads strided Q and K
+    # and the codes it writes are contiguous
+    g = torch.Generator().manual_seed(18)
+    big = [torch.randn((2, 300, 5, 128), generator=g).to(torch.bfloat16) for _ in range(3)]
+    q, k, v = (t[:, :, 1:4, :] for t in big)
+    qd, kd, vd = (t.cuda()[:, :, 1:4, :] for t in big)
+    assert not qd.is_contiguous()
+    st = new_status()
+    rp, ci = sa.sa_route(qd, kd, 70, 1.0, dev_status=st)
+    o = torch.empty((2, 300, 3, 128), dtype=torch.bfloat16, device="cuda")
+    o, lse = sa.sa_attn_sparse(qd, kd, vd, rp, ci, o=o, qk_format="fp8", dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    rpn = to_np(rp).astype(np.int64)
+    cin = to_np(ci).astype(np.int64)[: rpn[-1]]
+    o_ref, lse_ref = oracle.attn_fp8_ref(q, k, v, rpn, cin)
+    l2, mx, _ = out_errors(to_np(o), o_ref)
+    assert l2 <= L2_TOL and mx <= MAXABS_TOL, (l2, mx)
+    assert lse_ok(to_np(lse), lse_ref)
+    check_codes(sa, q.contiguous(), k.contiguous())
+
+
+@pytest.mark.parametrize("q_block", [64, 128])
+def test_fp8_prepare_then_run_equals_attn_sparse(sa, q_block):
+    # the two halves (the quantiser runs in sa_attn_run) give the one-call
+    # result bit for bit
+    cfg, q, k, v = sa_inputs.make_inputs("mid")
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    st = new_status()
+    rp, ci = sa.sa_route(qd, kd, cfg.P, cfg.tau, q_block=q_block, dev_status=st)
+    o, lse = sa.sa_attn_sparse(qd, kd, vd, rp, ci, q_block=q_block, qk_format="fp8",
+                               dev_status=st)
+    p = sa.make_params(qd, kd, vd, o, q_block=q_block, qk_format="fp8")
+    ws = torch.empty(sa.sa_attn_workspace_bytes(p), dtype=torch.uint8, device="cuda")
+    sa.sa_attn_prepare(vd, rp, ci, workspace=ws, q_block=q_block, qk_format="fp8",
+                       dev_status=st)
+    o2, lse2 = sa.sa_attn_run(qd, kd, rp, ci, workspace=ws, v_like=vd, q_block=q_block,
+                              qk_format="fp8", dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert torch.equal(o.view(torch.int16), o2.view(torch.int16))
+    assert torch.equal(lse.view(torch.int32), lse2.view(torch.int32))

@@ -43,6 +43,30 @@ __device__ __forceinline__ float bf16_to_f32(uint16_t h) {
   return __uint_as_float(static_cast<uint32_t>(h) << 16);
 }
 
+// Two fp32 lanes in one 64-bit register: IEEE round-to-nearest adds and
+// subtracts of each lane, subnormals kept (no flush), so each lane rounds
+// exactly as the scalar __fadd_rn / __fsub_rn would.
+__device__ __forceinline__ uint64_t add2_rn(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t sub2_rn(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+// two_sum on both lanes of a pair (the same operations, lane by lane)
+__device__ __forceinline__ void two_sum2(uint64_t& s, uint64_t& e, uint64_t b) {
+  const uint64_t a = s;
+  const uint64_t t = add2_rn(a, b);
+  const uint64_t bb = sub2_rn(t, a);
+  const uint64_t err = add2_rn(sub2_rn(a, sub2_rn(t, bb)), sub2_rn(b, bb));
+  s = t;
+  e = add2_rn(e, err);
+}
+
 // TwoSum: s + e == a + b exactly (round-to-nearest, no overflow).
 __device__ __forceinline__ void two_sum(float& s, float& e, float b) {
   const float a = s;
@@ -133,9 +157,11 @@ __global__ void __launch_bounds__(128) pool_kernel(RouteArgs a) {
   const int t0 = i * blk;
   const int n = min(blk, a.S - t0);
 
-  float s[8], c[8];
+  // running sums and error terms of the 8 channels as 4 lane pairs
+  // (channels 2v, 2v + 1 in pair v), summed with two_sum2
+  uint64_t s2[4], c2[4];
 #pragma unroll
-  for (int u = 0; u < 8; ++u) s[u] = c[u] = 0.f;
+  for (int v = 0; v < 4; ++v) s2[v] = c2[v] = 0ull;
 
   if (active) {
     const uint16_t* base = X + b * st[0] + h * st[2] + d + t0 * st[1];
@@ -150,12 +176,21 @@ __global__ void __launch_bounds__(128) pool_kernel(RouteArgs a) {
           const uint32_t w[4] = {buf[u].x, buf[u].y, buf[u].z, buf[u].w};
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
-            two_sum(s[2 * v], c[2 * v], bf16_to_f32(static_cast<uint16_t>(w[v] & 0xffffu)));
-            two_sum(s[2 * v + 1], c[2 * v + 1], bf16_to_f32(static_cast<uint16_t>(w[v] >> 16)));
+            // the two bf16 of the word as fp32 (exact): low half, high half
+            const uint64_t x = (static_cast<uint64_t>(w[v] & 0xffff0000u) << 32) | (w[v] << 16);
+            two_sum2(s2[v], c2[v], x);
           }
         }
       }
     }
+  }
+  float s[8], c[8];
+#pragma unroll
+  for (int v = 0; v < 4; ++v) {
+    s[2 * v] = __uint_as_float(static_cast<uint32_t>(s2[v]));
+    s[2 * v + 1] = __uint_as_float(static_cast<uint32_t>(s2[v] >> 32));
+    c[2 * v] = __uint_as_float(static_cast<uint32_t>(c2[v]));
+    c[2 * v + 1] = __uint_as_float(static_cast<uint32_t>(c2[v] >> 32));
   }
   store_pooled<D>(a, which, b, h, d, i, nrow, n, s, c, active);
 }
@@ -521,6 +556,7 @@ __global__ void __launch_bounds__(256) select_kernel(RouteArgs a) {
         cnt += __popc(m);
       }
     } else {
+#pragma unroll 4
     for (int w = 0; w < a.words; ++w) {
       const int j = w * 32 + lane;
       bool keep = false;
@@ -675,36 +711,38 @@ __global__ void __launch_bounds__(kRecheckThreads) recheck_kernel(RouteArgs a) {
 // one CTA of 1024 threads: row_ptr = exclusive scan of the counts of the
 // CSR rows (each the count of its routed row).
 __global__ void __launch_bounds__(1024) scan_kernel(RouteArgs a) {
+  // one CTA; the rows are taken 1024 at a time (one count per thread, so the
+  // loads and stores are coalesced), each pass scanned across the CTA and
+  // offset by the running total of the passes before it
   __shared__ int64_t wsum[32];
   const int64_t n = a.L.rows;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int64_t per = (n + 1023) / 1024;
-  const int64_t lo = min(n, tid * per), hi = min(n, lo + per);
   const int* counts = ws_ptr<int>(a.ws, a.L.counts);
-  int64_t local = 0;
-  for (int64_t r = lo; r < hi; ++r) local += counts[routed_row(a, r)];
-  int64_t incl = local;
-  for (int off = 1; off < 32; off <<= 1) {
-    const int64_t v = __shfl_up_sync(0xffffffffu, incl, off);
-    if (lane >= off) incl += v;
-  }
-  if (lane == 31) wsum[warp] = incl;
-  __syncthreads();
-  if (warp == 0) {
-    int64_t v = wsum[lane];
+  int64_t carry = 0;
+  for (int64_t r0 = 0; r0 < n; r0 += 1024) {
+    const int64_t r = r0 + tid;
+    const int64_t c = r < n ? counts[routed_row(a, r)] : 0;
+    int64_t incl = c;
     for (int off = 1; off < 32; off <<= 1) {
-      const int64_t u = __shfl_up_sync(0xffffffffu, v, off);
-      if (lane >= off) v += u;
+      const int64_t v = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += v;
     }
-    wsum[lane] = v;  // inclusive over warps
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+      int64_t v = wsum[lane];
+      for (int off = 1; off < 32; off <<= 1) {
+        const int64_t u = __shfl_up_sync(0xffffffffu, v, off);
+        if (lane >= off) v += u;
+      }
+      wsum[lane] = v;  // inclusive over warps
+    }
+    __syncthreads();
+    if (r < n) a.row_ptr[r] = static_cast<int32_t>(carry + incl - c + (warp > 0 ? wsum[warp - 1] : 0));
+    carry += wsum[31];
+    __syncthreads();   // wsum is rewritten by the next pass
   }
-  __syncthreads();
-  int64_t run = incl - local + (warp > 0 ? wsum[warp - 1] : 0);
-  for (int64_t r = lo; r < hi; ++r) {
-    a.row_ptr[r] = static_cast<int32_t>(run);
-    run += counts[routed_row(a, r)];
-  }
-  if (tid == 1023) a.row_ptr[n] = static_cast<int32_t>(wsum[31]);
+  if (tid == 0) a.row_ptr[n] = static_cast<int32_t>(carry);
 }
 
 // ---------------------------------------------------------------- emit ---

@@ -719,9 +719,13 @@ __global__ void __launch_bounds__(1024) scan_kernel(RouteArgs a) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int* counts = ws_ptr<int>(a.ws, a.L.counts);
   int64_t carry = 0;
+  // each pass loads the next pass's count before scanning its own, so the
+  // global-load latency overlaps the scan
+  int64_t c_next = tid < n ? counts[routed_row(a, tid)] : 0;
   for (int64_t r0 = 0; r0 < n; r0 += 1024) {
     const int64_t r = r0 + tid;
-    const int64_t c = r < n ? counts[routed_row(a, r)] : 0;
+    const int64_t c = c_next;
+    c_next = r + 1024 < n ? counts[routed_row(a, r + 1024)] : 0;
     int64_t incl = c;
     for (int off = 1; off < 32; off <<= 1) {
       const int64_t v = __shfl_up_sync(0xffffffffu, incl, off);

@@ -357,6 +357,23 @@ def _sampled_attention_check(sa, cfg, q, k, v, rp, ci, seed, dense=False):
     assert lse_ok(lg, lrf)
 
 
+@pytest.mark.parametrize("dense", [False, True])
+def test_head_dim_64_with_several_tiles_per_cta(sa, dense):
+    # The other D = 64 cases fit in one tile per persistent CTA; here about
+    # four tiles run on each (313 key blocks, 157 pairs x 4 heads), so the
+    # D = 64 kernel's walks, O reuse and per-tile barrier phases are crossed
+    # from tile to tile; the last block is ragged (19 tokens).
+    S, H, D, P, tau = 19987, 4, 64, 300, 1.0
+    q, k, v = sa_inputs.random_small(S, H, D, seed=64)
+    cfg = sa_inputs.Config("d64", S=S, P=P, H=H, D=D, tau=tau, kind="iid")
+    assert cfg.Nb == 313
+    if dense:
+        _sampled_attention_check(sa, cfg, q, k, v, None, None, seed=65, dense=True)
+    else:
+        ref, rp, ci = check_route(sa, q, k, P, tau)
+        _sampled_attention_check(sa, cfg, q, k, v, ref["row_ptr"], ref["col_idx"], seed=66)
+
+
 def test_release_route_bitexact(sa, release):
     cfg, q, k, v = release
     ref, rp, ci = check_route(sa, q, k, cfg.P, cfg.tau)

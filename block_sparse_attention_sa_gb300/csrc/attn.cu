@@ -37,7 +37,10 @@
 // earlier). Each warpgroup keeps its own partial row sum; the two threads of
 // a row add them in the epilogue. The running max moves only when a block
 // max exceeds it by more than 2^14 (then O is rescaled, after the last PV
-// into it has completed).
+// into it has completed). The block maxima come with the S loads themselves
+// (the reduction form of tcgen05.ld returns each 32-column maximum), so the
+// chain from S to the exponentials holds no maximum instructions of its own
+// except in the ragged last key block, which is masked first.
 //
 // Warps: 0-3 softmax of even steps, 4-7 of odd steps, 8 producer (Q, and K and
 // V through one ring of stages in the order the MMA warp consumes them),
@@ -719,13 +722,18 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const uint32_t e0 = inf[2 * j], e1 = two ? inf[2 * j + 1] : 0u;
         const bool mem0 = (e0 >> qh) & 1u, mem1 = two && ((e1 >> qh) & 1u);
         uint32_t sr[128];
+        // the loads also return each 32-column maximum; the ragged last key
+        // block is masked first and takes its maximum in software
+        const bool tail0 = static_cast<int>(e0 >> 2) == Nb - 1;
+        const bool tail1 = two && static_cast<int>(e1 >> 2) == Nb - 1;
+        float hm0 = -INFINITY, hm1 = -INFINITY, hm2 = -INFINITY, hm3 = -INFINITY;
         if (mem0) {
-          tmem_ld32(lane_base + s_col, sr);
-          tmem_ld32(lane_base + s_col + 32, sr + 32);
+          tmem_ld32_max(lane_base + s_col, sr, hm0);
+          tmem_ld32_max(lane_base + s_col + 32, sr + 32, hm1);
         }
         if (mem1) {
-          tmem_ld32(lane_base + s_col + 64, sr + 64);
-          tmem_ld32(lane_base + s_col + 96, sr + 96);
+          tmem_ld32_max(lane_base + s_col + 64, sr + 64, hm2);
+          tmem_ld32_max(lane_base + s_col + 96, sr + 96, hm3);
         }
         // exp2-domain factor of each key block's logits: the softmax scale,
         // times 2^(e_q + e_k) with 8-bit scores (exact: powers of two)
@@ -737,16 +745,28 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           if (mem0) {
             reg_fence32(sr);
             reg_fence32(sr + 32);
-            mask_tail32(sr, e0, 0, Nb, last_valid);
-            mask_tail32(sr + 32, e0, 1, Nb, last_valid);
-            mx0 = fmaxf(max32(sr), max32(sr + 32));
+            reg_fence_f(hm0);
+            reg_fence_f(hm1);
+            if (tail0) {
+              mask_tail32(sr, e0, 0, Nb, last_valid);
+              mask_tail32(sr + 32, e0, 1, Nb, last_valid);
+              mx0 = fmaxf(max32(sr), max32(sr + 32));
+            } else {
+              mx0 = fmaxf(hm0, hm1);
+            }
           }
           if (mem1) {
             reg_fence32(sr + 64);
             reg_fence32(sr + 96);
-            mask_tail32(sr + 64, e1, 0, Nb, last_valid);
-            mask_tail32(sr + 96, e1, 1, Nb, last_valid);
-            mx1 = fmaxf(max32(sr + 64), max32(sr + 96));
+            reg_fence_f(hm2);
+            reg_fence_f(hm3);
+            if (tail1) {
+              mask_tail32(sr + 64, e1, 0, Nb, last_valid);
+              mask_tail32(sr + 96, e1, 1, Nb, last_valid);
+              mx1 = fmaxf(max32(sr + 64), max32(sr + 96));
+            } else {
+              mx1 = fmaxf(hm2, hm3);
+            }
           }
         }
         // the factors are positive: the max commutes with them

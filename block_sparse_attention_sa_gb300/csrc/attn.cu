@@ -712,20 +712,26 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       for (int j = (gs ^ sm) & 1; j < n_steps; j += kSets) {
         const int g = gs + j, sb = g % kSBuf;
         const uint32_t s_col = kColS + sb * 128;
+        // the step's walk entries (and with 8-bit scores its scale factors)
+        // do not depend on S: read them before waiting for it
+        const bool two = 2 * j + 1 < n;             // an odd walk's last step has one block
+        const uint32_t e0 = inf[2 * j], e1 = two ? inf[2 * j + 1] : 0u;
+        const bool mem0 = (e0 >> qh) & 1u, mem1 = two && ((e1 >> qh) & 1u);
+        // the loads also return each 32-column maximum; the ragged last key
+        // block is masked first and takes its maximum in software
+        const bool tail0 = static_cast<int>(e0 >> 2) == Nb - 1;
+        const bool tail1 = two && static_cast<int>(e1 >> 2) == Nb - 1;
+        // exp2-domain factor of each key block's logits: the softmax scale,
+        // times 2^(e_q + e_k) with 8-bit scores (exact: powers of two)
+        const float c0 = kF8 ? ldexpf(cl2, eq + kx[2 * j]) : cl2;
+        const float c1 = kF8 ? (two ? ldexpf(cl2, eq + kx[2 * j + 1]) : cl2) : cl2;
         if (!mbar_wait_warp(bar(L::bSFull + sb), (g / kSBuf) & 1, abort_sig)) {
           if (lane == 0) fail(kSiteSFull);
           stop = true;
           break;
         }
         tc_fence_after();
-        const bool two = 2 * j + 1 < n;             // an odd walk's last step has one block
-        const uint32_t e0 = inf[2 * j], e1 = two ? inf[2 * j + 1] : 0u;
-        const bool mem0 = (e0 >> qh) & 1u, mem1 = two && ((e1 >> qh) & 1u);
         uint32_t sr[128];
-        // the loads also return each 32-column maximum; the ragged last key
-        // block is masked first and takes its maximum in software
-        const bool tail0 = static_cast<int>(e0 >> 2) == Nb - 1;
-        const bool tail1 = two && static_cast<int>(e1 >> 2) == Nb - 1;
         float hm0 = -INFINITY, hm1 = -INFINITY, hm2 = -INFINITY, hm3 = -INFINITY;
         if (mem0) {
           tmem_ld32_max(lane_base + s_col, sr, hm0);
@@ -735,10 +741,6 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           tmem_ld32_max(lane_base + s_col + 64, sr + 64, hm2);
           tmem_ld32_max(lane_base + s_col + 96, sr + 96, hm3);
         }
-        // exp2-domain factor of each key block's logits: the softmax scale,
-        // times 2^(e_q + e_k) with 8-bit scores (exact: powers of two)
-        const float c0 = kF8 ? ldexpf(cl2, eq + kx[2 * j]) : cl2;
-        const float c1 = kF8 ? (two ? ldexpf(cl2, eq + kx[2 * j + 1]) : cl2) : cl2;
         float mx0 = -INFINITY, mx1 = -INFINITY;
         if (mem0 || mem1) {
           tmem_wait_ld();

@@ -583,10 +583,21 @@ sa_status sa_forward_host(const sa_params* p, const void* q_host, const void* k_
   // D2H on their own streams, compute on `stream`).
   // (lse is [B, H, S]: a head group's rows are one contiguous slice only for
   // B = 1, so a batched call that wants lse runs as a single group)
-  const int G = (p->B > 1 && lse_dev) ? 1 : std::max(1, std::min(kHostGroups, p->H / 8));
+  // The groups shrink toward the end: a copy of a head slice moves rows of
+  // (heads x D x 2) bytes, and the link carries wide rows faster (about 133
+  // GB/s at 1 KB, 180 at 2 KB, 200 at 3.5 KB, 211 contiguous), so the first
+  // groups are a quarter of the heads each; the last two (a seventh and the
+  // rest) keep short the tail in which nothing is left to copy in.
+  constexpr int kSched = 5;
+  static_assert(kSched <= kHostGroups, "head-group schedule exceeds the events");
+  const int G = ((p->B > 1 && lse_dev) || p->H < 16) ? 1 : kSched;
   const size_t row_bytes = static_cast<size_t>(p->H) * p->D * 2;   // one token, all heads
   const size_t rows = static_cast<size_t>(p->B) * p->S;
-  auto head0 = [&](int g) { return static_cast<int>(static_cast<int64_t>(p->H) * g / G); };
+  // group boundaries at 0, 1/4, 1/2, 3/4, 25/28 and 1 of the heads
+  auto head0 = [&](int g) {
+    static const int num[kSched + 1] = {0, 7, 14, 21, 25, 28};
+    return G == 1 ? (g == 0 ? 0 : p->H) : static_cast<int>((static_cast<int64_t>(p->H) * num[g] + 14) / 28);
+  };
   if (cudaEventRecord(hp->start, st) != cudaSuccess ||
       cudaStreamWaitEvent(hp->h2d, hp->start, 0) != cudaSuccess ||
       cudaStreamWaitEvent(hp->d2h, hp->start, 0) != cudaSuccess)

@@ -357,7 +357,9 @@ sa_status sa_attn_dense(const sa_params* p, const void* q, const void* k,
  * (host, pinned for asynchronous copies) to the device buffers, routes,
  * attends, and copies o (and lse if both lse pointers are non-NULL) back,
  * then returns without synchronising. The work is split into groups of
- * heads (up to 8 groups of at least 8 heads; one group for B > 1 with lse):
+ * heads (for H >= 16 five groups, a quarter of the heads each and then a
+ * seventh and the rest, since wide head slices copy faster and narrow last
+ * groups shorten the tail; one group for H < 16 or for B > 1 with lse):
  * each group is routed and attended as soon as its q, k, v slices have
  * landed, and its o slice is copied back as soon as it is done, so the
  * copies overlap the compute. Compute runs on `stream`; the copies run on two

@@ -357,6 +357,18 @@ def _sampled_attention_check(sa, cfg, q, k, v, rp, ci, seed, dense=False):
     assert lse_ok(lg, lrf)
 
 
+@pytest.mark.parametrize("S,H", [(341 * 64, 3), (256 * 64, 4), (205 * 64, 5), (683 * 64 - 7, 3)])
+def test_route_row_counts_around_the_scan_passes(sa, S, H):
+    # row_ptr is a scan over the route's H * Nb rows taken 1024 rows per pass:
+    # 1023, 1024, 1025 and 2049 rows put the last pass just short of, exactly
+    # at and just past a pass boundary; the CSR must be well formed and
+    # encode the oracle's route in every row (outside the tie window)
+    q, k, _ = sa_inputs.random_small(S, H, 64, seed=S + H)
+    Nb = oracle.num_blocks(S)
+    assert H * Nb in (1023, 1024, 1025, 2049)
+    check_route(sa, q, k, 100, 1.0)
+
+
 @pytest.mark.parametrize("dense", [False, True])
 def test_head_dim_64_with_several_tiles_per_cta(sa, dense):
     # The other D = 64 cases fit in one tile per persistent CTA; here about
